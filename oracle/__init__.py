@@ -1,0 +1,190 @@
+"""Plain CPU oracle for the W12 verify path (ctypes wrapper around w12_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline leg (and its ``--impl reference`` arm) are the only
+callers.  The CUDA library never imports or links this package.
+
+Every function cites the passage it follows: the SpecPilot summary page
+(onedev.kr/papers/1654), section "What's different" (무엇과 다른가), for the W12
+format, the 8-bit Q-pass view and greedy tree acceptance.  The readings taken
+where that passage is silent are listed at the top of ``w12_oracle.c``.
+
+Multi-core helpers split rows over Python threads; ctypes releases the GIL
+during each foreign call, so the threads run the plain C loops in parallel.
+The arithmetic in each thread is unchanged.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+BUILD = os.path.join(HERE, "_build")
+SO = os.path.join(BUILD, "libw12oracle.so")
+# A test may point this at a deliberately broken build of w12_oracle.c to check
+# that the pins catch the mistake.
+OVERRIDE_ENV = "W12_ORACLE_SO"
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build() -> str:
+    os.makedirs(BUILD, exist_ok=True)
+    src = os.path.join(HERE, "w12_oracle.c")
+    if not os.path.exists(SO) or os.path.getmtime(src) > os.path.getmtime(SO):
+        tmp = SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                               "-o", tmp, src])
+        os.replace(tmp, SO)
+    return SO
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(os.environ.get(OVERRIDE_ENV) or build())
+            p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+            lib.w12o_base.argtypes = [p, i64]
+            lib.w12o_base.restype = ctypes.c_int
+            lib.w12o_encode.argtypes = [p, i64, i64, p, p, p, p, p, i64]
+            lib.w12o_encode.restype = i64
+            lib.w12o_decode.argtypes = [i64, i64, p, p, p, p, p, p]
+            lib.w12o_decode.restype = None
+            lib.w12o_decode_q8.argtypes = [i64, i64, p, p, p, p, p]
+            lib.w12o_decode_q8.restype = None
+            lib.w12o_gemm.argtypes = [p, i64, i64, p, i64, p, i64, p]
+            lib.w12o_gemm.restype = None
+            lib.w12o_argmax.argtypes = [p, i64, i64, p, p]
+            lib.w12o_argmax.restype = None
+            lib.w12o_accept.argtypes = [p, p, p, i32, p, p]
+            lib.w12o_accept.restype = i32
+            _lib = lib
+        return _lib
+
+
+def _p(a: np.ndarray | None) -> int | None:
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class Encoded:
+    """Canonical W12 encoding of an N x K matrix (the layout the oracle defines)."""
+
+    def __init__(self, N, K, hi, lo, base, rowptr, esc):
+        self.N, self.K = N, K
+        self.hi, self.lo, self.base, self.rowptr, self.esc = hi, lo, base, rowptr, esc
+
+    @property
+    def n_esc(self) -> int:
+        return int(self.esc.size)
+
+    def storage_bits(self) -> int:
+        """Bits stored: 12 per weight, 32 per escape, 32 per rowptr entry, 8 per base."""
+        return self.hi.size * 8 + (self.N * self.K) * 4 + self.esc.size * 32 + self.rowptr.size * 32 + self.base.size * 8
+
+
+def base_of_row(row) -> int:
+    """Window base of one channel (fullest 16-binade window, lowest base on ties)."""
+    row = _c(row, np.uint16)
+    return int(_L().w12o_base(_p(row), row.size))
+
+
+def encode(W) -> Encoded:
+    """Encode an N x K bf16 (uint16 bits) matrix into the canonical W12 planes."""
+    W = _c(W, np.uint16)
+    N, K = W.shape
+    lib = _L()
+    n_esc = int(lib.w12o_encode(_p(W), N, K, None, None, None, None, None, 0))
+    hi = np.empty((N, K), np.uint8)
+    lo = np.empty((N, (K + 1) // 2), np.uint8)
+    base = np.empty(N, np.uint8)
+    rowptr = np.empty(N + 1, np.uint32)
+    esc = np.empty(max(n_esc, 1), np.uint32)
+    got = int(lib.w12o_encode(_p(W), N, K, _p(hi), _p(lo), _p(base), _p(rowptr), _p(esc), n_esc))
+    assert got == n_esc
+    return Encoded(N, K, hi, lo, base, rowptr, esc[:n_esc].copy())
+
+
+def decode(enc: Encoded) -> np.ndarray:
+    out = np.empty((enc.N, enc.K), np.uint16)
+    esc = enc.esc if enc.esc.size else np.zeros(1, np.uint32)
+    _L().w12o_decode(enc.N, enc.K, _p(enc.hi), _p(enc.lo), _p(enc.base), _p(enc.rowptr), _p(esc), _p(out))
+    return out
+
+
+def decode_q8(enc: Encoded) -> np.ndarray:
+    out = np.empty((enc.N, enc.K), np.uint16)
+    esc = enc.esc if enc.esc.size else np.zeros(1, np.uint32)
+    _L().w12o_decode_q8(enc.N, enc.K, _p(enc.hi), _p(enc.base), _p(enc.rowptr), _p(esc), _p(out))
+    return out
+
+
+def gemm(x, W, threads: int | None = None, with_bound: bool = True):
+    """fp64 y[M,N] = x[M,K] . W[N,K]^T (k increasing) and B = sum |x*w|.
+
+    W holds bf16 bits of the decoded weights.  Rows of W are split over threads."""
+    x = _c(x, np.uint16)
+    W = _c(W, np.uint16)
+    M, K = x.shape
+    N = W.shape[0]
+    y = np.empty((M, N), np.float64)
+    B = np.empty((M, N), np.float64) if with_bound else None
+    lib = _L()
+    nt = max(1, min(threads or (os.cpu_count() or 1), N))
+    bounds = [(N * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        a, b = bounds[i], bounds[i + 1]
+        if b > a:
+            lib.w12o_gemm(_p(x), M, K, W.ctypes.data + a * K * 2, b - a, y.ctypes.data + a * 8, N,
+                          None if B is None else B.ctypes.data + a * 8)
+
+    if nt == 1:
+        run(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(nt)))
+    return (y, B) if with_bound else y
+
+
+def argmax(logits):
+    """Row argmax (lowest index on ties, NaN below all) and the top-1 minus top-2 gap."""
+    logits = _c(logits, np.float64)
+    M, V = logits.shape
+    idx = np.empty(M, np.int32)
+    gap = np.empty(M, np.float64)
+    _L().w12o_argmax(_p(logits), M, V, _p(idx), _p(gap))
+    return idx, gap
+
+
+def accept(tok, parent, draft):
+    """Greedy acceptance on one tree: (L, path nodes root..a*, bonus); L = -1 if invalid."""
+    tok = _c(tok, np.int32)
+    parent = _c(parent, np.int32)
+    draft = _c(draft, np.int32)
+    n = parent.size
+    path = np.full(max(n, 1), -1, np.int32)
+    bonus = np.zeros(1, np.int32)
+    L = int(_L().w12o_accept(_p(tok), _p(parent), _p(draft), n, _p(path), _p(bonus)))
+    if L < 0:
+        return -1, np.zeros(0, np.int32), -1
+    return L, path[: L + 1].copy(), int(bonus[0])
+
+
+def accept_batched(tok, parent, draft, offsets):
+    """Acceptance for several trees concatenated; offsets[r]..offsets[r+1] is request r."""
+    res = []
+    for r in range(len(offsets) - 1):
+        a, b = int(offsets[r]), int(offsets[r + 1])
+        res.append(accept(tok[a:b], parent[a:b], draft[a:b]))
+    return res

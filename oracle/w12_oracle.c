@@ -1,0 +1,231 @@
+/*
+ * w12_oracle.c - plain CPU oracle for the W12 verify path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or constant generator with the CUDA library, and the CUDA
+ * library never calls it.
+ *
+ * Source of every definition below: the SpecPilot summary page
+ * (onedev.kr/papers/1654), section "What's different" (무엇과 다른가), which
+ * describes W12 as: per channel, pick the 16-binade interval in which the
+ * weights cluster; store sign 1 bit, exponent offset 4 bits and mantissa
+ * 7 bits in 12 bits; restore values outside the interval, zeros and denormals
+ * exactly from a per-channel sparse escape list; the two-level verification
+ * Q pass reads an 8-bit view of the front of the W12 record; acceptance is
+ * greedy along the draft tree with a bonus token.  Where that paragraph is
+ * silent this file takes the plainest reading:
+ *   - record r = s<<11 | (E-base)<<7 | m   (s: sign bit, E: 8-bit exponent
+ *     field, m: 7-bit mantissa of the bf16 value);
+ *   - stored as a hi plane (r >> 4, one byte per weight: the 8-bit front view)
+ *     and a lo plane (r & 0xF, two weights per byte, even k in the low nibble);
+ *   - the window is [base, base+15] with base in 1..239 (normal exponents
+ *     only); the fullest window wins, ties go to the lowest base, and a row
+ *     with no normal value gets base 1;
+ *   - E = 0 (zeros, denormals) and E = 255 (Inf, NaN) are always escapes;
+ *   - an escape entry is one u32: col<<16 | raw bf16 bits, entries of a row
+ *     sorted by col, rows delimited by rowptr[N+1]; the record slot of an
+ *     escaped weight holds r = 0;
+ *   - the 8-bit view truncates: the low 4 mantissa bits read as zero;
+ *     escapes stay exact in that view.
+ * Arithmetic is fp64 with sums taken in increasing k.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static int exponent_field(uint16_t w) { return (w >> 7) & 0xFF; }
+
+/* Window choice for one channel: hist[E] over normal values, then the first
+ * base with the strictly largest count of E in [base, base+15]. */
+int w12o_base(const uint16_t* row, int64_t K) {
+  int64_t hist[256];
+  memset(hist, 0, sizeof(hist));
+  for (int64_t k = 0; k < K; ++k) {
+    int E = exponent_field(row[k]);
+    if (E >= 1 && E <= 254) hist[E] += 1;
+  }
+  int best_base = 1;
+  int64_t best_count = -1;
+  for (int b = 1; b <= 239; ++b) {
+    int64_t count = 0;
+    for (int E = b; E <= b + 15; ++E) count += hist[E];
+    if (count > best_count) {
+      best_count = count;
+      best_base = b;
+    }
+  }
+  return best_base;
+}
+
+/* True when weight w is stored as a 12-bit record under window base. */
+static int in_window(uint16_t w, int base) {
+  int E = exponent_field(w);
+  return E >= 1 && E <= 254 && E >= base && E <= base + 15;
+}
+
+/* Encode an N x K bf16 matrix.  hi[N*K], lo[N*ceil(K/2)], base[N], rowptr[N+1];
+ * esc may be NULL (count only).  Returns the number of escapes, or -1 when
+ * esc_cap is too small. */
+int64_t w12o_encode(const uint16_t* W, int64_t N, int64_t K, uint8_t* hi, uint8_t* lo, uint8_t* base,
+                    uint32_t* rowptr, uint32_t* esc, int64_t esc_cap) {
+  int64_t lo_row = (K + 1) / 2;
+  int64_t n_esc = 0;
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = W + n * K;
+    int b = w12o_base(row, K);
+    if (base) base[n] = (uint8_t)b;
+    if (rowptr) rowptr[n] = (uint32_t)n_esc;
+    if (lo) memset(lo + n * lo_row, 0, (size_t)lo_row);
+    for (int64_t k = 0; k < K; ++k) {
+      uint16_t w = row[k];
+      uint32_t r;
+      if (in_window(w, b)) {
+        uint32_t s = (w >> 15) & 1u;
+        uint32_t eo = (uint32_t)(exponent_field(w) - b);
+        uint32_t m = w & 0x7Fu;
+        r = (s << 11) | (eo << 7) | m;
+      } else {
+        r = 0;
+        if (esc) {
+          if (n_esc >= esc_cap) return -1;
+          esc[n_esc] = ((uint32_t)k << 16) | w;
+        }
+        n_esc += 1;
+      }
+      if (hi) hi[n * K + k] = (uint8_t)(r >> 4);
+      if (lo) lo[n * lo_row + k / 2] |= (uint8_t)((r & 0xFu) << ((k & 1) ? 4 : 0));
+    }
+  }
+  if (rowptr) rowptr[N] = (uint32_t)n_esc;
+  return n_esc;
+}
+
+/* Record of weight (n, k) from the two planes. */
+static uint32_t record_at(const uint8_t* hi, const uint8_t* lo, int64_t K, int64_t n, int64_t k) {
+  int64_t lo_row = (K + 1) / 2;
+  uint32_t h = hi[n * K + k];
+  uint32_t l = (lo[n * lo_row + k / 2] >> ((k & 1) ? 4 : 0)) & 0xFu;
+  return (h << 4) | l;
+}
+
+/* Decode: in-window weights from their record and the channel base, escaped
+ * weights from the escape list.  q8 != 0 gives the 8-bit front view. */
+static void decode_impl(int64_t N, int64_t K, const uint8_t* hi, const uint8_t* lo, const uint8_t* base,
+                        const uint32_t* rowptr, const uint32_t* esc, uint16_t* out, int q8) {
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t k = 0; k < K; ++k) {
+      uint32_t r = q8 ? ((uint32_t)hi[n * K + k] << 4) : record_at(hi, lo, K, n, k);
+      uint32_t s = (r >> 11) & 1u;
+      uint32_t eo = (r >> 7) & 0xFu;
+      uint32_t m = r & 0x7Fu;
+      out[n * K + k] = (uint16_t)((s << 15) | ((base[n] + eo) << 7) | m);
+    }
+    for (uint32_t e = rowptr[n]; e < rowptr[n + 1]; ++e) {
+      int64_t col = esc[e] >> 16;
+      out[n * K + col] = (uint16_t)(esc[e] & 0xFFFFu);
+    }
+  }
+}
+
+void w12o_decode(int64_t N, int64_t K, const uint8_t* hi, const uint8_t* lo, const uint8_t* base,
+                 const uint32_t* rowptr, const uint32_t* esc, uint16_t* out) {
+  decode_impl(N, K, hi, lo, base, rowptr, esc, out, 0);
+}
+
+void w12o_decode_q8(int64_t N, int64_t K, const uint8_t* hi, const uint8_t* base, const uint32_t* rowptr,
+                    const uint32_t* esc, uint16_t* out) {
+  decode_impl(N, K, hi, NULL, base, rowptr, esc, out, 1);
+}
+
+static double bf16_value(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* y[m*ldy + n] = sum_k x[m,k] * W[n,k] in fp64, k increasing; bound[m*ldy + n]
+ * = sum_k |x[m,k] * W[n,k]| (may be NULL).  W holds N rows of K bf16 values. */
+void w12o_gemm(const uint16_t* x, int64_t M, int64_t K, const uint16_t* W, int64_t N, double* y, int64_t ldy,
+               double* bound) {
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, mag = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double p = bf16_value(x[m * K + k]) * bf16_value(W[n * K + k]);
+        acc += p;
+        mag += p < 0 ? -p : p;
+      }
+      y[m * ldy + n] = acc;
+      if (bound) bound[m * ldy + n] = mag;
+    }
+  }
+}
+
+/* Ordering used by argmax: NaN ranks below every number, -0 equals +0. */
+static int better(double a, double b) {
+  if (a != a) return 0;
+  if (b != b) return 1;
+  return a > b;
+}
+
+/* Row-wise argmax of an M x V matrix; ties go to the lowest index.  gap[m] =
+ * value at the argmax minus the largest value at any other index (+inf when
+ * V == 1); may be NULL. */
+void w12o_argmax(const double* logits, int64_t M, int64_t V, int32_t* idx, double* gap) {
+  for (int64_t m = 0; m < M; ++m) {
+    const double* row = logits + m * V;
+    int64_t best = 0;
+    for (int64_t v = 1; v < V; ++v)
+      if (better(row[v], row[best])) best = v;
+    idx[m] = (int32_t)best;
+    if (gap) {
+      int64_t second = -1;
+      for (int64_t v = 0; v < V; ++v) {
+        if (v == best) continue;
+        if (second < 0 || better(row[v], row[second])) second = v;
+      }
+      gap[m] = second < 0 ? 1.0 / 0.0 : row[best] - row[second];
+    }
+  }
+}
+
+/* Greedy acceptance on one draft tree of n nodes (node 0 = root, parent[0] =
+ * -1, parent[i] < i).  tok[i] is the target's greedy token after node i;
+ * draft[i] is node i's drafted token (draft[0] unused).  Node i is accepted
+ * when its parent is accepted and draft[i] == tok[parent[i]].  The answer is
+ * the deepest accepted node (lowest index among equals), the root-to-node
+ * path, and the bonus token tok[node].  Writes the path (root first) to
+ * path_nodes[0..L] and returns L, the number of accepted draft tokens; returns
+ * -1 for an invalid tree. */
+int32_t w12o_accept(const int32_t* tok, const int32_t* parent, const int32_t* draft, int32_t n, int32_t* path_nodes,
+                    int32_t* bonus) {
+  if (n < 1 || parent[0] != -1) return -1;
+  int32_t* acc = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+  int32_t* depth = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+  acc[0] = 1;
+  depth[0] = 0;
+  int32_t best = 0;
+  for (int32_t i = 1; i < n; ++i) {
+    int32_t p = parent[i];
+    if (p < 0 || p >= i) {
+      free(acc);
+      free(depth);
+      return -1;
+    }
+    acc[i] = acc[p] && draft[i] == tok[p];
+    depth[i] = depth[p] + 1;
+    if (acc[i] && depth[i] > depth[best]) best = i;
+  }
+  int32_t L = depth[best];
+  int32_t v = best;
+  for (int32_t j = L; j >= 0; --j) {
+    path_nodes[j] = v;
+    v = parent[v];
+  }
+  *bonus = tok[best];
+  free(acc);
+  free(depth);
+  return L;
+}

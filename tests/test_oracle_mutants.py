@@ -1,0 +1,56 @@
+"""Each plausible mistake planted in the oracle's C source must fail a pin.
+
+The mutant is compiled on the CPU into a temporary library and the pin suite
+(test_oracle_pins.py) runs against it in a child process; the child must
+report a failure.  This shows the pins constrain every step of the oracle:
+window choice, record layout, planes, decode, the 8-bit view, the fp64 GEMM
+and its bound, argmax ties and tree acceptance.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "w12_oracle.c")
+
+MUTANTS = {
+    "window ties go high": ("if (count > best_count) {", "if (count >= best_count) {"),
+    "window range short": ("for (int b = 1; b <= 239; ++b) {", "for (int b = 1; b <= 238; ++b) {"),
+    "window 15 binades": ("for (int E = b; E <= b + 15; ++E) count += hist[E];",
+                          "for (int E = b; E <= b + 14; ++E) count += hist[E];"),
+    "record drops sign": ("r = (s << 11) | (eo << 7) | m;", "r = (eo << 7) | m;"),
+    "record sign misplaced": ("r = (s << 11) | (eo << 7) | m;", "r = (s << 10) | (eo << 7) | m;"),
+    "lo nibble order swapped": ("lo[n * lo_row + k / 2] |= (uint8_t)((r & 0xFu) << ((k & 1) ? 4 : 0));",
+                                "lo[n * lo_row + k / 2] |= (uint8_t)((r & 0xFu) << ((k & 1) ? 0 : 4));"),
+    "decode exponent off by one": ("((base[n] + eo) << 7)", "((base[n] + eo + 1) << 7)"),
+    "q8 rounds up": ("uint32_t r = q8 ? ((uint32_t)hi[n * K + k] << 4)", "uint32_t r = q8 ? (((uint32_t)hi[n * K + k] << 4) | 8u)"),
+    "escape drops sign": ("esc[n_esc] = ((uint32_t)k << 16) | w;", "esc[n_esc] = ((uint32_t)k << 16) | (w & 0x7FFFu);"),
+    "gemm reversed k": ("double p = bf16_value(x[m * K + k]) * bf16_value(W[n * K + k]);",
+                        "double p = bf16_value(x[m * K + (K - 1 - k)]) * bf16_value(W[n * K + k]);"),
+    "gemm sign flip": ("acc += p;", "acc -= p;"),
+    "gemm bound signed": ("mag += p < 0 ? -p : p;", "mag += p;"),
+    "argmax ties go high": ("  return a > b;\n}", "  return a >= b;\n}"),
+    "accept compares own token": ("acc[i] = acc[p] && draft[i] == tok[p];", "acc[i] = acc[p] && draft[i] == tok[i];"),
+    "accept ignores parent": ("acc[i] = acc[p] && draft[i] == tok[p];", "acc[i] = draft[i] == tok[p];"),
+    "accept depth ties go high": ("if (acc[i] && depth[i] > depth[best]) best = i;",
+                                  "if (acc[i] && depth[i] >= depth[best]) best = i;"),
+    "bonus from parent": ("*bonus = tok[best];", "*bonus = tok[parent[best] < 0 ? 0 : parent[best]];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {name}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o", str(so), str(mut)])
+    env = dict(os.environ, W12_ORACLE_SO=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant '{name}' survived the pins:\n{r.stdout[-2000:]}"

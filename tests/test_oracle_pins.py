@@ -1,0 +1,331 @@
+"""Pins of the CPU oracle to facts fixed by the pages and by mathematics.
+
+The W12 facts come from the SpecPilot summary page (onedev.kr/papers/1654),
+section "What's different": lossless restoration of every value (zeros and
+denormals included), the fullest 16-binade window per channel, 12 bits per
+weight plus the escape overhead, the 8-bit front view used by the Q pass, and
+greedy acceptance with a bonus token.  Each test below checks the oracle
+against something other than its own formula: exhaustive round trips, brute
+force, hand-worked fixtures, closed forms and library routines.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def f32_of_bf16(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_of_f32(f):
+    """Round-to-nearest-even float32 -> bf16 bits (finite inputs)."""
+    u = np.asarray(f, np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def exponent(bits):
+    return (np.asarray(bits, np.uint16) >> 7) & 0xFF
+
+
+# ----------------------------------------------------------------------------- round trip
+
+@pytest.mark.parametrize("target_base", [1, 2, 60, 100, 112, 120, 127, 200, 239])
+def test_roundtrip_every_bf16_pattern(target_base):
+    """decode(encode(w)) == w bit for bit for all 65,536 bf16 patterns (±0,
+    denormals, Inf and NaN payloads included), each row forced to a window
+    base by a dominant block of filler values inside [base, base+15]."""
+    filler = []
+    for E in range(target_base, target_base + 16):
+        for i in range(600):
+            filler.append(((i & 1) << 15) | (E << 7) | (i % 128))
+    filler = np.array(filler, np.uint16)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(16, 4096)
+    W = np.concatenate([pats, np.broadcast_to(filler, (16, filler.size))], axis=1)
+    enc = oracle.encode(W)
+    assert np.all(enc.base == target_base)
+    dec = oracle.decode(enc)
+    assert np.array_equal(dec, W)
+    # every pattern outside the window (or E in {0, 255}) is an escape, and only those
+    E = exponent(W)
+    outside = (E == 0) | (E == 255) | (E < target_base) | (E > target_base + 15)
+    assert enc.n_esc == int(outside.sum())
+    cols = enc.esc >> 16
+    raws = (enc.esc & 0xFFFF).astype(np.uint16)
+    rows = np.repeat(np.arange(16), np.diff(enc.rowptr.astype(np.int64)))
+    assert np.array_equal(W[rows, cols], raws)
+    assert np.all(outside[rows, cols])
+
+
+def test_roundtrip_generated_matrix():
+    import synth
+    W = synth.weights(0, 0, 0, 512, 256)
+    enc = oracle.encode(W)
+    assert np.array_equal(oracle.decode(enc), W)
+
+
+# ----------------------------------------------------------------------------- window choice
+
+def brute_force_base(row):
+    """Count normal values in every legal window directly; fullest, lowest base."""
+    E = exponent(row).astype(np.int64)
+    normal = (E >= 1) & (E <= 254)
+    best, best_b = -1, None
+    for b in range(1, 240):
+        c = int(np.sum(normal & (E >= b) & (E <= b + 15)))
+        if c > best:
+            best, best_b = c, b
+    return best_b, best
+
+
+def test_window_matches_brute_force_on_tiny_rows():
+    rng = np.random.default_rng(1234)
+    for trial in range(400):
+        K = int(rng.integers(1, 65))
+        centre = int(rng.integers(1, 255))
+        spread = int(rng.integers(0, 60))
+        E = np.clip(rng.integers(centre - spread, centre + spread + 1, K), 0, 255)
+        if trial % 7 == 0:
+            E[rng.random(K) < 0.3] = 0          # zeros / denormals
+        if trial % 11 == 0:
+            E[rng.random(K) < 0.2] = 255        # Inf / NaN
+        row = ((rng.integers(0, 2, K) << 15) | (E << 7) | rng.integers(0, 128, K)).astype(np.uint16)
+        b_ref, count = brute_force_base(row)
+        b = oracle.base_of_row(row)
+        assert b == b_ref, (trial, b, b_ref)
+        enc = oracle.encode(row[None, :])
+        assert K - enc.n_esc == count          # in-window values are exactly the fullest window's count
+
+
+@pytest.mark.parametrize("E0,expect", [(127, 112), (5, 1), (1, 1), (16, 1), (17, 2), (254, 239), (200, 185)])
+def test_window_single_binade(E0, expect):
+    """All values share one exponent: every window holding it ties, the lowest wins."""
+    row = np.array([(E0 << 7) | m for m in range(20)], np.uint16)
+    assert oracle.base_of_row(row) == expect
+
+
+def test_window_two_clusters():
+    far = np.array([100 << 7] * 10 + [140 << 7] * 20, np.uint16)        # 40 binades apart: larger cluster wins
+    assert oracle.base_of_row(far) == 125
+    near = np.array([100 << 7] * 10 + [110 << 7] * 20, np.uint16)       # both fit: lowest window holding both
+    assert oracle.base_of_row(near) == 95
+    no_normal = np.array([0x0000, 0x8000, 0x0001, 0x807F], np.uint16)
+    assert oracle.base_of_row(no_normal) == 1
+
+
+# ----------------------------------------------------------------------------- golden fixtures
+
+def _hex_list(s):
+    return [int(t, 16) for t in s.split()] if s.strip() else []
+
+
+def load_record_fixture():
+    rows, q8 = {}, {}
+    for line in open(os.path.join(GOLDEN, "w12_records.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = [p.strip() for p in line.split("|")]
+        if parts[0].startswith("q8"):
+            q8[int(parts[0].split()[1])] = _hex_list(parts[1])
+            continue
+        esc = [(int(c), int(r, 16)) for c, r in (t.split(":") for t in parts[5].split())]
+        rows[int(parts[0])] = dict(w=_hex_list(parts[1]), base=int(parts[2]), hi=_hex_list(parts[3]),
+                                   lo=_hex_list(parts[4]), esc=esc)
+    return rows, q8
+
+
+def test_golden_records():
+    rows, q8 = load_record_fixture()
+    for r, case in rows.items():
+        enc = oracle.encode(np.array([case["w"]], np.uint16))
+        assert int(enc.base[0]) == case["base"], r
+        assert enc.hi[0].tolist() == case["hi"], r
+        assert enc.lo[0].tolist() == case["lo"], r
+        got = [(int(e >> 16), int(e & 0xFFFF)) for e in enc.esc]
+        assert got == case["esc"], r
+        assert oracle.decode(enc)[0].tolist() == case["w"], r
+        assert oracle.decode_q8(enc)[0].tolist() == q8[r], r
+
+
+# ----------------------------------------------------------------------------- size
+
+def test_bits_per_weight_is_12_plus_escape_overhead():
+    import synth
+    for (N, K) in [(512, 256), (64, 5120), (7, 33)]:
+        W = synth.weights(0, 3, 1, N, K)
+        enc = oracle.encode(W)
+        # escapes counted independently of the encoder, from the chosen bases
+        E = exponent(W).astype(np.int64)
+        b = enc.base.astype(np.int64)[:, None]
+        outside = (E == 0) | (E == 255) | (E < b) | (E > b + 15)
+        assert enc.n_esc == int(outside.sum())
+        bits = 12 * N * K + 32 * enc.n_esc + 32 * (N + 1) + 8 * N
+        assert enc.storage_bits() == bits
+        assert enc.hi.size == N * K and enc.lo.size == N * ((K + 1) // 2)
+
+
+def test_bits_per_weight_on_gaussian_rows_is_in_the_pages_range():
+    """Plain per-channel Gaussian weights (no injected outliers) land at
+    12.01-12.02 bits/weight, the range the pages report for 8 dense models."""
+    rng = np.random.default_rng(7)
+    N, K = 256, 5120
+    s = np.exp(rng.uniform(np.log(0.005), np.log(0.05), N)).astype(np.float32)
+    W = bf16_of_f32(rng.standard_normal((N, K)).astype(np.float32) * s[:, None])
+    enc = oracle.encode(W)
+    bpw = enc.storage_bits() / (N * K)
+    assert 12.005 < bpw < 12.02, bpw
+
+
+# ----------------------------------------------------------------------------- Q8 view
+
+def test_q8_closed_form():
+    import synth
+    W = synth.weights(0, 0, 1, 300, 200)
+    enc = oracle.encode(W)
+    q = oracle.decode_q8(enc)
+    E = exponent(W).astype(np.int64)
+    b = enc.base.astype(np.int64)[:, None]
+    inwin = (E >= 1) & (E <= 254) & (E >= b) & (E <= b + 15)
+    assert np.array_equal(q[inwin], W[inwin] & 0xFFF0)
+    assert np.array_equal(q[~inwin], W[~inwin])
+    wf, qf = np.abs(f32_of_bf16(W[inwin])).astype(np.float64), np.abs(f32_of_bf16(q[inwin])).astype(np.float64)
+    assert np.all(qf <= wf)
+    assert np.all((wf - qf) / wf < 2.0 ** -3)
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+def test_gemm_one_hot_selects_a_column():
+    import synth
+    W = synth.weights(0, 0, 0, 64, 96)
+    for k0 in [0, 17, 95]:
+        x = np.zeros((1, 96), np.uint16)
+        x[0, k0] = 0x3F80                       # 1.0
+        y, B = oracle.gemm(x, W, threads=1)
+        assert np.array_equal(y[0], f32_of_bf16(W[:, k0]).astype(np.float64))
+        assert np.array_equal(B[0], np.abs(y[0]))
+
+
+def test_gemm_exact_on_small_integers():
+    rng = np.random.default_rng(3)
+    M, N, K = 5, 37, 203
+    xi = rng.integers(-8, 9, (M, K))
+    wi = rng.integers(-8, 9, (N, K))
+    y, B = oracle.gemm(bf16_of_f32(xi.astype(np.float32)), bf16_of_f32(wi.astype(np.float32)), threads=3)
+    assert np.array_equal(y, (xi @ wi.T).astype(np.float64))
+    assert np.array_equal(B, (np.abs(xi) @ np.abs(wi).T).astype(np.float64))
+
+
+def test_gemm_matches_numpy_float64():
+    import synth
+    W = synth.weights(0, 1, 2, 70, 300)
+    x = synth.activations(1, 1, 2, 6, 300)
+    y, B = oracle.gemm(x, W, threads=4)
+    xf, wf = f32_of_bf16(x).astype(np.float64), f32_of_bf16(W).astype(np.float64)
+    assert np.allclose(y, xf @ wf.T, rtol=0, atol=1e-12 * B.max())
+    assert np.allclose(B, np.abs(xf) @ np.abs(wf).T, rtol=1e-12)
+    assert np.all(B >= np.abs(y))
+
+
+# ----------------------------------------------------------------------------- argmax
+
+def test_argmax_ties_lowest_index_and_gap():
+    L = np.array([[1.0, 3.0, 3.0, 2.0],
+                  [-0.0, 0.0, -1.0, -2.0],
+                  [np.nan, -np.inf, -5.0, np.nan],
+                  [7.0, np.nan, 7.5, 7.25]])
+    idx, gap = oracle.argmax(L)
+    assert idx.tolist() == [1, 0, 2, 2]
+    assert gap[0] == 0.0 and gap[1] == 0.0 and gap[3] == 0.25
+
+
+def test_argmax_matches_numpy():
+    rng = np.random.default_rng(5)
+    L = rng.standard_normal((9, 1000))
+    idx, gap = oracle.argmax(L)
+    assert np.array_equal(idx, np.argmax(L, axis=1))
+    s = np.sort(L, axis=1)
+    assert np.allclose(gap, s[:, -1] - s[:, -2])
+
+
+# ----------------------------------------------------------------------------- acceptance
+
+def brute_force_accept(tok, parent, draft):
+    """Walk every root-to-leaf path while draft == target token at the parent;
+    best = max by (depth, -node)."""
+    n = len(parent)
+    children = {i: [] for i in range(n)}
+    for i in range(1, n):
+        children[int(parent[i])].append(i)
+    leaves = [i for i in range(n) if not children[i]]
+    best = (0, 0)
+    for leaf in leaves:
+        path = [leaf]
+        while path[-1] != 0:
+            path.append(int(parent[path[-1]]))
+        path = path[::-1]
+        for d in range(1, len(path)):
+            if draft[path[d]] != tok[path[d - 1]]:
+                break
+            if (d, -path[d]) > (best[0], -best[1]):
+                best = (d, path[d])
+    node = best[1]
+    path = [node]
+    while path[-1] != 0:
+        path.append(int(parent[path[-1]]))
+    return best[0], path[::-1], int(tok[node])
+
+
+def load_tree_fixture():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "tree_cases.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        p = [s.strip() for s in line.split("|")]
+        ints = lambda s: [int(t) for t in s.split()] if s != "-" else []
+        cases.append(dict(name=p[0], parent=ints(p[1]), tok=ints(p[2]), draft=ints(p[3]), L=int(p[4]),
+                          path=ints(p[5]), bonus=int(p[6])))
+    return cases
+
+
+def test_golden_trees():
+    for c in load_tree_fixture():
+        L, path, bonus = oracle.accept(c["tok"], c["parent"], c["draft"])
+        assert L == c["L"], c["name"]
+        if L >= 0:
+            assert path.tolist() == c["path"] and bonus == c["bonus"], c["name"]
+
+
+def test_accept_matches_brute_force_on_random_trees():
+    import synth
+    rng = np.random.default_rng(11)
+    for t in range(600):
+        n = int(rng.integers(1, 40))
+        V = int(rng.choice([2, 3, 4, 1024]))
+        parent = synth.tree(2, t, 0, n)
+        tok = rng.integers(0, V, n).astype(np.int32)
+        draft = rng.integers(0, V, n).astype(np.int32)
+        # plant: half the nodes copy the target token at their parent
+        plant = rng.random(n) < 0.6
+        for i in range(1, n):
+            if plant[i]:
+                draft[i] = tok[parent[i]]
+        L, path, bonus = oracle.accept(tok, parent, draft)
+        Lb, pathb, bonusb = brute_force_accept(tok, parent, draft)
+        assert (L, path.tolist(), bonus) == (Lb, pathb, bonusb), t
+
+
+def test_accept_chain_all_match_gives_full_depth():
+    for n in [1, 2, 8, 33]:
+        parent = np.arange(-1, n - 1, dtype=np.int32)
+        tok = np.arange(100, 100 + n, dtype=np.int32)
+        draft = np.concatenate([[0], tok[:-1]]).astype(np.int32)
+        L, path, bonus = oracle.accept(tok, parent, draft)
+        assert L == n - 1 and path.tolist() == list(range(n)) and bonus == tok[-1]
