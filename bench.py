@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the W12 verify path on one GB300 (or N replicas under torchrun).
+
+A step is one verify pass of the 27B-class dense block at M = 16 draft-tree
+rows: the four W12 decode-fused GEMMs (fused QKV 7168x5120, O 5120x5120,
+gate/up 34816x5120, down 5120x17408) launched in dependency order.  Weights
+are generated on the device from the seeded generator, W12-encoded once
+(offline, untimed) and stay resident; the block's 506 MB of W12 records is
+larger than L2, so no flush is needed between steps.
+
+The JSON line reports decoded-weight GB/s (2 bytes per weight per step), the
+roofline of the GEMM kernel against the measured HBM copy bandwidth, the
+end-to-end figure through the public API with host buffers, the CPU oracle
+timed on a bounded sample, SM clocks sampled during the timed region, and
+(under "rows") the other hot-path rows timed in the same run: the Q8 pass over
+the same block and the 151936x5120 LM head with fused argmax and tree
+acceptance.
+
+--impl reference times the CPU oracle (the plain C reference of the method)
+on the same workload and metric, a bounded sample of rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+BLOCK = [("qkv", 7168, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
+LMHEAD = (151936, 5120)
+WORKLOAD = ("27B-class dense block: fused QKV 7168x5120, O 5120x5120, gate/up 34816x5120, "
+            "down 5120x17408; W12 weights (per-channel N(0,s_c), s_c log-uniform [0.005,0.05], "
+            "0.5% outliers x2^9, 0.2% zeros, 0.1% denormals); M=16 bf16 N(0,1) rows")
+HBM_FALLBACK = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["w12", "reference"], default="w12")
+    p.add_argument("--M", type=int, default=16)
+    p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                          ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in rows):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------ CPU oracle timing
+
+def oracle_block_sample(M: int, rows_per_matrix: int, layer: int = 0, threads: int | None = None):
+    """Oracle work on a bounded sample of the block: decode (from the canonical
+    W12 planes) and fp64 GEMM of `rows_per_matrix` channels of each matrix.
+    Returns (seconds, weights processed, threads used)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    threads = threads or (os.cpu_count() or 1)
+    prepared = []
+    for tensor, (_, N, K) in enumerate(BLOCK):
+        rows = np.arange(rows_per_matrix) * (N // rows_per_matrix)
+        W = synth.weight_rows(0, layer, tensor, K, rows)
+        prepared.append((oracle.encode(W), synth.activations(1, layer, tensor, M, K)))
+    t0 = time.perf_counter()
+    n = 0
+    for enc, x in prepared:
+        Wd = oracle.decode(enc)
+        oracle.gemm(x, Wd, threads=threads, with_bound=False)
+        n += Wd.size
+    return time.perf_counter() - t0, n, threads
+
+
+def calibrate_rows(M: int, target_s: float) -> int:
+    rows = 64
+    dt, _, _ = oracle_block_sample(M, rows)
+    while dt < target_s / 4 and rows < 8192:
+        rows *= 2
+        dt, _, _ = oracle_block_sample(M, rows)
+    return max(32, int(rows * target_s / max(dt, 1e-3)))
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step decodes and multiplies a
+    bounded sample of the block's channels at M rows."""
+    if rank != 0:
+        return
+    rows = calibrate_rows(args.M, target_s=0.25)
+    for _ in range(args.warmup):
+        oracle_block_sample(args.M, rows)
+    total_t, total_w = 0.0, 0
+    threads = os.cpu_count() or 1
+    for _ in range(args.steps):
+        dt, n, threads = oracle_block_sample(args.M, rows)
+        total_t += dt
+        total_w += n
+    value = 2.0 * total_w / total_t / 1e9
+    sample = f"{rows} channels of each block matrix per step (decode + fp64 GEMM at M={args.M})"
+    line = {"impl": "reference", "metric": "W12 verify-GEMM decoded-weight GB/s", "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": args.M, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+
+def encode_block(w12, synth, torch, layer: int):
+    mats = []
+    for tensor, (name, N, K) in enumerate(BLOCK):
+        W = torch.empty((N, K), dtype=torch.int16, device="cuda")
+        synth.weights_dev(0, layer, tensor, W)
+        A = w12.encode(W)
+        del W
+        mats.append((name, A))
+    torch.cuda.empty_cache()
+    return mats
+
+
+def run_w12(args, world, rank, local):
+    import torch
+
+    import lossless_bit_weights_gb300 as w12
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M = args.M
+    mats = encode_block(w12, synth, torch, layer=0)
+    xs, ys = [], []
+    for tensor, (name, A) in enumerate(mats):
+        x = torch.empty((M, A.K), dtype=torch.int16, device=dev)
+        synth.activations_dev(1, 0, tensor, x)
+        xs.append(x)
+        ys.append(torch.empty((M, A.N), dtype=torch.float32, device=dev))
+    ws = w12.Workspace(dev)
+    ws.get(max(w12.gemm_workspace_size(M, A.N, A.K) for _, A in mats))
+    weights = sum(A.N * A.K for _, A in mats)
+    stream_bytes = sum(A.stream_bytes() + 2 * M * A.K + 4 * M * A.N for _, A in mats)
+    stored = sum(A.stored_bytes() for _, A in mats)
+    n_esc = sum(A.n_esc for _, A in mats)
+
+    def step():
+        for (_, A), x, y in zip(mats, xs, ys):
+            w12.w12_gemm(x, A, y=y, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: per-launch events on the launching stream
+    K = args.steps
+    s = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mats) + 1)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(s)
+    for k in range(K):
+        e = evs[k]
+        for i, ((_, A), x, y) in enumerate(zip(mats, xs, ys)):
+            e[i].record(s)
+            w12.w12_gemm(x, A, y=y, ws=ws)
+        e[len(mats)].record(s)
+    t1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_mat_ms = [statistics.fmean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)) for i in range(len(mats))]
+    kernel_ms = sum(per_mat_ms)
+
+    value = world * 2.0 * weights * K / (elapsed_ms * 1e-3) / 1e9
+    hbm, hbm_kind = peaks()
+    achieved = stream_bytes / (kernel_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    xh = [torch.empty_like(x, device="cpu").pin_memory() for x in xs]
+    for x, h in zip(xs, xh):
+        h.copy_(x.cpu())
+    yh = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+
+    def e2e_step():
+        for (_, A), x, y, h, hy in zip(mats, xs, ys, xh, yh):
+            x.copy_(h, non_blocking=True)
+            w12.w12_gemm(x, A, y=y, ws=ws)
+            hy.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    Ke = max(1, K // 2)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    h2d = sum(x.numel() * 2 for x in xs)
+    d2h = sum(y.numel() * 4 for y in ys)
+    e2e = {"value": world * 2.0 * weights * Ke / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    rows = None
+    if not args.no_rows:
+        rows = extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm)
+
+    del mats
+    torch.cuda.empty_cache()
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        r = calibrate_rows(M, target_s=2.0)
+        dt, n, threads = oracle_block_sample(M, r)
+        cpu = {"value": 2.0 * n / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{r} channels of each block matrix: decode + fp64 GEMM at M={M} ({dt:.1f} s wall)"}
+
+    if rank == 0:
+        line = {
+            "metric": "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "weights_per_step": weights, "stored_bytes": stored,
+                       "bits_per_weight": 8.0 * stored / weights, "escape_fraction": n_esc / weights,
+                       "us_per_layer": 1e3 * elapsed_ms / K, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: 506 MB of W12 per step, larger than the 129 MB L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "peak_kind": hbm_kind,
+                         "kernel": "k_gemm<NB=2,Q8=0,EPI=store> (4 launches/step)",
+                         "per_matrix_us": {n: 1e3 * t for (n, _), t in zip(BLOCK_NAMES, per_mat_ms)}},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")} | {"samples": clk["samples"]},
+            "gpu_launches": len(BLOCK) * K,
+        }
+        if rows is not None:
+            line["rows"] = rows
+        print(json.dumps(line), flush=True)
+
+
+BLOCK_NAMES = [(n, (N, K)) for n, N, K in BLOCK]
+
+
+def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
+    """Q8 pass over the same block and the LM head with fused argmax + tree
+    acceptance, each timed with CUDA events (not part of `value`)."""
+    out = {}
+    s = torch.cuda.current_stream()
+    steps = max(5, args.steps // 4)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(n):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    ysq = [torch.empty((M, A.N), dtype=torch.float32, device="cuda") for _, A in mats]
+
+    def q8_step():
+        for (_, A), x, y in zip(mats, xs, ysq):
+            w12.w12_gemm_q8(x, A, y=y, ws=ws)
+
+    ms = timed(q8_step, steps)
+    weights = sum(A.N * A.K for _, A in mats)
+    qbytes = sum(A.stream_bytes(q8=True) + 2 * M * A.K + 4 * M * A.N for _, A in mats)
+    out["q8_block_m16"] = {"us": 1e3 * ms, "decoded_GBps": 2 * weights / (ms * 1e-3) / 1e9,
+                           "stream_GBps": qbytes / (ms * 1e-3) / 1e9, "frac_hbm": qbytes / (ms * 1e-3) / 1e9 / hbm}
+
+    V, K = LMHEAD
+    W = torch.empty((V, K), dtype=torch.int16, device="cuda")
+    synth.weights_dev(0, 0, 9, W)
+    H = w12.encode(W)
+    del W
+    torch.cuda.empty_cache()
+    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    synth.activations_dev(1, 0, 9, x)
+    import numpy as np
+    parent = torch.from_numpy(synth.tree(2, 0, 1, M)).cuda()
+    draft = torch.from_numpy(synth.drafts(3, 0, 1, M, V)).cuda()
+    ws2 = w12.Workspace()
+    ms = timed(lambda: w12.w12_lmhead_verify(x, H, parent, draft, ws=ws2), steps)
+    hb = H.stream_bytes() + 2 * M * K
+    out["lmhead_verify_m16"] = {"us": 1e3 * ms, "decoded_GBps": 2 * V * K / (ms * 1e-3) / 1e9,
+                                "stream_GBps": hb / (ms * 1e-3) / 1e9, "frac_hbm": hb / (ms * 1e-3) / 1e9 / hbm}
+    del H
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_w12(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * w12.h - C ABI of the W12 verify-path library (libw12.so, sm_103a).
+ *
+ * W12 is the lossless 12-bit weight format of the SpecPilot summary page
+ * (onedev.kr/papers/1654), section "What's different" (무엇과 다른가): for
+ * each output channel the 16-binade exponent window holding the most weights
+ * is chosen; an in-window bf16 weight is stored as sign 1 bit, exponent
+ * offset 4 bits and mantissa 7 bits; values outside the window, zeros and
+ * denormals are restored exactly from a per-channel sparse escape list.  The
+ * same paragraph describes the GEMM that decodes the 12-bit records in
+ * registers behind the weight stream and stays deterministic with stream-K,
+ * the two-level verification Q pass over an 8-bit view of the front of the
+ * record, and the greedy acceptance of a draft tree plus a bonus token.  The
+ * page's "What it is" (무엇인가) section gives why this path matters: every
+ * tree node of a verify step reads the full target weights (80% of a 23.61 ms
+ * step).
+ *
+ * Record (canonical): r = s<<11 | (E-base)<<7 | m for a bf16 value with sign s,
+ * exponent field E and mantissa m; base is in 1..239; E = 0 (zeros,
+ * denormals) and E = 255 (Inf, NaN) always escape; the 8-bit view is r >> 4
+ * and reads the low 4 mantissa bits as zero (escapes stay exact).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every call
+ *  - Status: each call returns W12_OK (0) or one of the W12_ERR_* codes; the
+ *    thread-local w12_last_error() then holds a one-line reason.  Nothing is
+ *    thrown across the ABI.  Argument checks happen on the host before any
+ *    launch; a call that fails them touches no memory.
+ *  - Memory: every pointer argument is device memory owned by the caller,
+ *    except where a parameter says "host".  No call allocates device memory;
+ *    calls that need scratch take a caller-owned workspace whose size is given
+ *    by the matching *_workspace_size query.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ *    device work is enqueued on it asynchronously; only w12_encode_plan
+ *    synchronises it (it returns the escape count to the host).
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - Shapes: 1 <= N, 1 <= K <= 65535 (the escape entry keeps the column in 16
+ *    bits and reserves the all-ones column), 1 <= M.
+ *
+ * Device layout of a W12 matrix (what w12_encode writes and the kernels read)
+ *  The matrix is cut into tiles of 32 channels x 64 columns: RT = ceil(N/32)
+ *  row tiles, KC = ceil(K/64) column chunks, tile index i = rt*KC + kc.  Rows
+ *  and columns past N and K hold record 0 and never escape.
+ *  - hi:  RT*KC tiles of 2048 bytes, the 8-bit front view (r >> 4) of each
+ *         weight.  In a tile, channel 8q+g and column 16t+j sit at byte
+ *         q*512 + (4g+t)*16 + 4*(j/4) + {0,2,1,3}[j%4].
+ *  - lo:  RT*KC tiles of 1024 bytes, the low nibble (r & 0xF).  Channel 8q+g,
+ *         column 16t+j sits in the 8-byte group at q*256 + (4g+t)*8, at bit
+ *         32*(p/4) + 4*(p%4) + 16*(j%2) of that group, p = 2*(j/4) + (j%4)/2.
+ *  - base: N bytes, the window base of each channel.
+ *  - esc_tile_ptr: RT*KC+1 u32, exclusive prefix of escape counts per tile.
+ *  - esc: n_esc u32 entries, grouped by tile and sorted by (channel, column)
+ *         within a tile: raw bf16 | (column-in-chunk) << 16 | (channel-in-tile) << 22.
+ *  w12_export_canonical converts to the canonical planes for comparison.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W12_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define W12_API __attribute__((visibility("default")))
+#else
+#define W12_API
+#endif
+
+typedef enum w12_status {
+  W12_OK = 0,
+  W12_ERR_INVALID_ARG = 1,      /* null pointer, negative count, bad stream use */
+  W12_ERR_SHAPE = 2,            /* N, K or M out of range */
+  W12_ERR_BUFFER_TOO_SMALL = 3, /* workspace smaller than the size query says */
+  W12_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  W12_ERR_BOUNDS = 5,           /* device data inconsistent with the descriptor */
+  W12_ERR_TIMEOUT = 6           /* reserved: no call waits on the device */
+} w12_status;
+
+/* A W12 matrix in device memory (layout above).  The struct itself lives in
+ * host memory; the library reads it during the call and keeps no reference. */
+typedef struct w12_matrix {
+  int64_t N, K;
+  uint8_t* hi;
+  uint8_t* lo;
+  uint8_t* base;
+  uint32_t* esc_tile_ptr;
+  uint32_t* esc;
+  int64_t n_esc;
+} w12_matrix;
+
+/* One-line reason for the last non-OK status on this host thread. */
+W12_API const char* w12_last_error(void);
+/* Name of a status code. */
+W12_API const char* w12_status_string(int status);
+/* W12_ABI_VERSION of the loaded library. */
+W12_API int w12_abi_version(void);
+
+/* ---- sizes (pure host functions, no CUDA calls) ------------------------- */
+
+/* Bytes of the hi plane, the lo plane, and tiles (RT*KC) of an N x K matrix;
+ * -1 for an invalid shape. */
+W12_API int64_t w12_hi_bytes(int64_t N, int64_t K);
+W12_API int64_t w12_lo_bytes(int64_t N, int64_t K);
+W12_API int64_t w12_tile_count(int64_t N, int64_t K);
+
+/* ---- encode (pages: "What's different", W12 conversion) ----------------- */
+
+/* Step 1 of 2.  Reads W[N*K] (bf16, row-major, channel n = row n), writes the
+ * window base of every channel to base[N] and the tile escape offsets to
+ * esc_tile_ptr[tile_count+1], and stores the total escape count in *n_esc
+ * (host pointer).  Synchronises `stream` to return the count. */
+W12_API int w12_encode_plan(const uint16_t* W, int64_t N, int64_t K, uint8_t* base, uint32_t* esc_tile_ptr,
+                    int64_t* n_esc, void* stream);
+
+/* Step 2 of 2.  A->base and A->esc_tile_ptr must hold step 1's output for the
+ * same W; A->hi, A->lo and A->esc (A->n_esc entries, may be NULL when 0) are
+ * written.  Asynchronous. */
+W12_API int w12_encode(const uint16_t* W, const w12_matrix* A, void* stream);
+
+/* ---- decode ------------------------------------------------------------- */
+
+/* Exact inverse of encode: W_out[N*K] bf16 row-major. */
+W12_API int w12_decode(const w12_matrix* A, uint16_t* W_out, void* stream);
+/* The 8-bit view: in-window weights with the low 4 mantissa bits cleared,
+ * escapes exact.  Reads only hi, base and the escapes. */
+W12_API int w12_decode_q8(const w12_matrix* A, uint16_t* W_out, void* stream);
+
+/* Canonical planes: hi_out[N*K] = r >> 4; lo_out[N*ceil(K/2)] with even
+ * columns in the low nibble; rowptr_out[N+1]; esc_out[n_esc] = col<<16 | raw,
+ * sorted by column within each channel.  Asynchronous. */
+W12_API int w12_export_canonical(const w12_matrix* A, uint8_t* hi_out, uint8_t* lo_out, uint32_t* rowptr_out,
+                         uint32_t* esc_out, void* stream);
+
+/* ---- verify GEMM (pages: "What's different", decode-fused stream-K GEMM) -- */
+
+/* Workspace bytes for w12_gemm / w12_gemm_q8 with these shapes on the current
+ * device.  The workspace's first w12_gemm_counter_bytes(N) bytes are tile
+ * counters that must be zero before the first call; every completed call
+ * leaves them zero again (re-zero after a failed call). */
+W12_API size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+W12_API size_t w12_gemm_counter_bytes(int64_t N);
+
+/* y[M*N] (fp32, row-major, token m = row m) = x[M*K] (bf16, row-major) times
+ * decode(A)^T, fp32 accumulation.  The K range is split over warps by a fixed
+ * partition and partial sums are added in a fixed order, so repeated calls
+ * give identical bits.  Asynchronous. */
+W12_API int w12_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Same, with the 8-bit view of the weights (the two-level verification Q
+ * pass).  Reads only hi, base and the escapes. */
+W12_API int w12_gemm_q8(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* ---- LM head with fused argmax ----------------------------------------- */
+
+/* Workspace bytes for the LM-head calls (same counter rule as w12_gemm). */
+W12_API size_t w12_lmhead_workspace_size(int64_t M, int64_t V, int64_t K);
+
+/* tok[M] = argmax over v of (x . decode(head)^T)[m, v]; the logits are never
+ * written to memory.  Ties go to the lowest v; NaN ranks below every number.
+ * head has N = V channels.  Asynchronous. */
+W12_API int w12_lmhead_argmax(const uint16_t* x, int64_t M, const w12_matrix* head, int32_t* tok, void* ws,
+                      size_t ws_bytes, void* stream);
+W12_API int w12_lmhead_argmax_q8(const uint16_t* x, int64_t M, const w12_matrix* head, int32_t* tok, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* LM-head argmax followed by tree acceptance (tree_verify_tokens semantics)
+ * in the same stream without a host round trip; tok[M] is also written. */
+W12_API int w12_lmhead_verify(const uint16_t* x, int64_t M, const w12_matrix* head, int q8, const int32_t* parent,
+                      const int32_t* draft, const int32_t* req_offsets, int32_t n_req, int32_t* tok,
+                      int32_t* path_len, int32_t* path_nodes, int32_t* bonus, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* ---- tree acceptance (pages: "What's different", greedy path + bonus) ---- */
+
+/* M tree nodes of n_req requests, request r owning nodes
+ * [req_offsets[r], req_offsets[r+1]) (req_offsets = NULL: one request of M
+ * nodes).  Node indices in parent[] and path_nodes[] are local to the
+ * request; parent[first] = -1 and 0 <= parent[i] < i otherwise.  tok[i] is
+ * the target's greedy token after node i, draft[i] node i's drafted token.
+ * Node i is accepted when its parent is and draft[i] == tok[parent[i]]; the
+ * deepest accepted node a* wins (lowest index among equals).  Outputs per
+ * request: path_len[r] = depth of a*, path_nodes[off_r .. off_r+L] = the
+ * root-to-a* path, bonus[r] = tok[a*].  An invalid tree or offset range gives
+ * path_len[r] = -1 and bonus[r] = -1.  path_nodes[off_r ..) beyond the path
+ * is scratch.  Asynchronous. */
+W12_API int tree_verify_tokens(const int32_t* tok, const int32_t* parent, const int32_t* draft,
+                       const int32_t* req_offsets, int32_t n_req, int64_t M, int32_t* path_len,
+                       int32_t* path_nodes, int32_t* bonus, void* stream);
+
+/* Same from fp32 logits[M*V]: the row argmax (same tie rule) gives tok;
+ * workspace >= tree_verify_workspace_size(M) bytes. */
+W12_API size_t tree_verify_workspace_size(int64_t M);
+W12_API int tree_verify(const float* logits, int64_t M, int64_t V, const int32_t* parent, const int32_t* draft,
+                const int32_t* req_offsets, int32_t n_req, int32_t* path_len, int32_t* path_nodes,
+                int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

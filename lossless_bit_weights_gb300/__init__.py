@@ -1,0 +1,300 @@
+"""Python binding of libw12 (the W12 verify-path C ABI in include/w12.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: if libw12.so cannot be built or loaded, every call raises.
+
+The names mirror the C functions: ``w12_encode_plan``/``w12_encode`` (wrapped
+together by :func:`encode`), :func:`w12_decode`, :func:`w12_decode_q8`,
+:func:`w12_gemm`, :func:`w12_gemm_q8`, :func:`w12_lmhead_argmax`,
+:func:`w12_lmhead_verify`, :func:`tree_verify_tokens`, :func:`tree_verify` and
+:func:`w12_export_canonical`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+W12_OK = 0
+STATUS_NAMES = {0: "W12_OK", 1: "W12_ERR_INVALID_ARG", 2: "W12_ERR_SHAPE", 3: "W12_ERR_BUFFER_TOO_SMALL",
+                4: "W12_ERR_CUDA", 5: "W12_ERR_BOUNDS", 6: "W12_ERR_TIMEOUT"}
+
+
+class W12Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class w12_matrix(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("hi", ctypes.c_void_p), ("lo", ctypes.c_void_p),
+                ("base", ctypes.c_void_p), ("esc_tile_ptr", ctypes.c_void_p), ("esc", ctypes.c_void_p),
+                ("n_esc", ctypes.c_int64)]
+
+
+# (name, restype, argtypes) of every exported symbol, in include/w12.h order.
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+_MP = ctypes.POINTER(w12_matrix)
+SIGNATURES = [
+    ("w12_last_error", ctypes.c_char_p, []),
+    ("w12_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("w12_abi_version", ctypes.c_int, []),
+    ("w12_hi_bytes", _I64, [_I64, _I64]),
+    ("w12_lo_bytes", _I64, [_I64, _I64]),
+    ("w12_tile_count", _I64, [_I64, _I64]),
+    ("w12_encode_plan", ctypes.c_int, [_P, _I64, _I64, _P, _P, ctypes.POINTER(_I64), _P]),
+    ("w12_encode", ctypes.c_int, [_P, _MP, _P]),
+    ("w12_decode", ctypes.c_int, [_MP, _P, _P]),
+    ("w12_decode_q8", ctypes.c_int, [_MP, _P, _P]),
+    ("w12_export_canonical", ctypes.c_int, [_MP, _P, _P, _P, _P, _P]),
+    ("w12_gemm_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w12_gemm_counter_bytes", _SZ, [_I64]),
+    ("w12_gemm", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_gemm_q8", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_lmhead_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w12_lmhead_argmax", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_lmhead_argmax_q8", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_lmhead_verify", ctypes.c_int, [_P, _I64, _MP, ctypes.c_int, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("tree_verify_tokens", ctypes.c_int, [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P]),
+    ("tree_verify_workspace_size", _SZ, [_I64]),
+    ("tree_verify", ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
+]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if the sources changed) libw12.so.  Raises on failure."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libw12.so missing at {path}")
+            L = ctypes.CDLL(path)
+            for name, res, args in SIGNATURES:
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(status: int) -> None:
+    if status != W12_OK:
+        raise W12Error(status, lib().w12_last_error().decode(errors="replace"))
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _bits16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"expected bf16 bits (bfloat16/int16/uint16), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t
+
+
+def _i32(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous int32 CUDA tensor")
+    return t
+
+
+class W12Matrix:
+    """Device buffers of one W12-encoded matrix (layout of include/w12.h)."""
+
+    def __init__(self, N, K, hi, lo, base, esc_tile_ptr, esc, n_esc):
+        self.N, self.K = int(N), int(K)
+        self.hi, self.lo, self.base, self.esc_tile_ptr, self.esc = hi, lo, base, esc_tile_ptr, esc
+        self.n_esc = int(n_esc)
+        self._desc = w12_matrix(self.N, self.K, _ptr(hi), _ptr(lo), _ptr(base), _ptr(esc_tile_ptr),
+                                _ptr(esc) if self.n_esc else None, self.n_esc)
+
+    def desc(self):
+        return ctypes.byref(self._desc)
+
+    @property
+    def device(self):
+        return self.hi.device
+
+    def stored_bytes(self) -> int:
+        """Bytes this matrix occupies on the device (planes, bases, escape index and escapes)."""
+        return (self.hi.numel() + self.lo.numel() + self.base.numel() + 4 * self.esc_tile_ptr.numel()
+                + 4 * self.n_esc)
+
+    def stream_bytes(self, q8: bool = False) -> int:
+        """Bytes one GEMM pass must read: records (1.5 or 1 B/weight on the tiled planes),
+        escapes (4 B each), the escape index and the bases."""
+        rec = self.hi.numel() + (0 if q8 else self.lo.numel())
+        return rec + 4 * self.n_esc + 4 * self.esc_tile_ptr.numel() + self.base.numel()
+
+
+def tile_count(N: int, K: int) -> int:
+    return int(lib().w12_tile_count(N, K))
+
+
+def encode(W: torch.Tensor, stream=None) -> W12Matrix:
+    """w12_encode_plan + w12_encode of an N x K bf16 matrix (synchronises the stream once)."""
+    W = _bits16(W)
+    N, K = W.shape
+    L = lib()
+    dev = W.device
+    T = int(L.w12_tile_count(N, K))
+    if T < 0:
+        raise W12Error(2, f"shape {N}x{K} out of range")
+    base = torch.empty(N, dtype=torch.uint8, device=dev)
+    tp = torch.empty(T + 1, dtype=torch.int32, device=dev)
+    n_esc = ctypes.c_int64(0)
+    s = _stream(stream)
+    _check(L.w12_encode_plan(_ptr(W), N, K, _ptr(base), _ptr(tp), ctypes.byref(n_esc), s))
+    hi = torch.empty(int(L.w12_hi_bytes(N, K)), dtype=torch.uint8, device=dev)
+    lo = torch.empty(int(L.w12_lo_bytes(N, K)), dtype=torch.uint8, device=dev)
+    esc = torch.empty(max(int(n_esc.value), 1), dtype=torch.int32, device=dev)
+    A = W12Matrix(N, K, hi, lo, base, tp, esc, n_esc.value)
+    _check(L.w12_encode(_ptr(W), A.desc(), s))
+    return A
+
+
+def w12_decode(A: W12Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out = torch.empty((A.N, A.K), dtype=torch.bfloat16, device=A.device) if out is None else _bits16(out)
+    _check(lib().w12_decode(A.desc(), _ptr(out), _stream(stream)))
+    return out
+
+
+def w12_decode_q8(A: W12Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out = torch.empty((A.N, A.K), dtype=torch.bfloat16, device=A.device) if out is None else _bits16(out)
+    _check(lib().w12_decode_q8(A.desc(), _ptr(out), _stream(stream)))
+    return out
+
+
+def w12_export_canonical(A: W12Matrix, stream=None) -> dict:
+    """Canonical planes: hi [N,K] u8, lo [N,ceil(K/2)] u8, rowptr [N+1] i32, esc [n_esc] i32."""
+    dev = A.device
+    hi = torch.empty((A.N, A.K), dtype=torch.uint8, device=dev)
+    lo = torch.empty((A.N, (A.K + 1) // 2), dtype=torch.uint8, device=dev)
+    rowptr = torch.empty(A.N + 1, dtype=torch.int32, device=dev)
+    esc = torch.empty(max(A.n_esc, 1), dtype=torch.int32, device=dev)
+    _check(lib().w12_export_canonical(A.desc(), _ptr(hi), _ptr(lo), _ptr(rowptr), _ptr(esc), _stream(stream)))
+    return dict(hi=hi, lo=lo, rowptr=rowptr, esc=esc[: A.n_esc], base=A.base)
+
+
+class Workspace:
+    """A zero-initialised device workspace that grows on demand (counters start at zero)."""
+
+    def __init__(self, device=None):
+        self.device = device or torch.device("cuda")
+        self.buf = torch.zeros(256, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if nbytes > self.buf.numel():
+            self.buf = torch.zeros(int(nbytes), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().w12_gemm_workspace_size(M, N, K))
+
+
+def lmhead_workspace_size(M: int, V: int, K: int) -> int:
+    return int(lib().w12_lmhead_workspace_size(M, V, K))
+
+
+def _gemm(fn, x, A, y, ws, stream):
+    x = _bits16(x)
+    M = x.shape[0]
+    if x.shape[1] != A.K:
+        raise ValueError(f"x has {x.shape[1]} columns, matrix has K={A.K}")
+    y = torch.empty((M, A.N), dtype=torch.float32, device=x.device) if y is None else y
+    ws = ws or Workspace(x.device)
+    need = gemm_workspace_size(M, A.N, A.K)
+    buf = ws.get(need)
+    _check(fn(_ptr(x), M, A.desc(), _ptr(y), _ptr(buf), buf.numel(), _stream(stream)))
+    return y
+
+
+def w12_gemm(x: torch.Tensor, A: W12Matrix, y: torch.Tensor | None = None, ws: Workspace | None = None,
+             stream=None) -> torch.Tensor:
+    """y[M,N] fp32 = x[M,K] bf16 . decode(A)^T."""
+    return _gemm(lib().w12_gemm, x, A, y, ws, stream)
+
+
+def w12_gemm_q8(x: torch.Tensor, A: W12Matrix, y: torch.Tensor | None = None, ws: Workspace | None = None,
+                stream=None) -> torch.Tensor:
+    """Same with the 8-bit view of the weights (Q pass)."""
+    return _gemm(lib().w12_gemm_q8, x, A, y, ws, stream)
+
+
+def w12_lmhead_argmax(x: torch.Tensor, head: W12Matrix, q8: bool = False, tok: torch.Tensor | None = None,
+                      ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    x = _bits16(x)
+    M = x.shape[0]
+    tok = torch.empty(M, dtype=torch.int32, device=x.device) if tok is None else tok
+    ws = ws or Workspace(x.device)
+    buf = ws.get(lmhead_workspace_size(M, head.N, head.K))
+    fn = lib().w12_lmhead_argmax_q8 if q8 else lib().w12_lmhead_argmax
+    _check(fn(_ptr(x), M, head.desc(), _ptr(tok), _ptr(buf), buf.numel(), _stream(stream)))
+    return tok
+
+
+def _tree_out(M, n_req, device):
+    return (torch.empty(n_req, dtype=torch.int32, device=device), torch.empty(M, dtype=torch.int32, device=device),
+            torch.empty(n_req, dtype=torch.int32, device=device))
+
+
+def w12_lmhead_verify(x, head: W12Matrix, parent, draft, req_offsets=None, q8: bool = False,
+                      ws: Workspace | None = None, stream=None):
+    """LM-head argmax + acceptance: returns (tok, path_len, path_nodes, bonus)."""
+    x = _bits16(x)
+    M = x.shape[0]
+    n_req = 1 if req_offsets is None else req_offsets.numel() - 1
+    tok = torch.empty(M, dtype=torch.int32, device=x.device)
+    path_len, path_nodes, bonus = _tree_out(M, n_req, x.device)
+    ws = ws or Workspace(x.device)
+    buf = ws.get(lmhead_workspace_size(M, head.N, head.K))
+    _check(lib().w12_lmhead_verify(_ptr(x), M, head.desc(), int(q8), _ptr(_i32(parent)), _ptr(_i32(draft)),
+                                   _ptr(req_offsets), n_req, _ptr(tok), _ptr(path_len), _ptr(path_nodes),
+                                   _ptr(bonus), _ptr(buf), buf.numel(), _stream(stream)))
+    return tok, path_len, path_nodes, bonus
+
+
+def tree_verify_tokens(tok, parent, draft, req_offsets=None, stream=None):
+    """Greedy acceptance from target tokens: returns (path_len, path_nodes, bonus)."""
+    M = tok.numel()
+    n_req = 1 if req_offsets is None else req_offsets.numel() - 1
+    path_len, path_nodes, bonus = _tree_out(M, n_req, tok.device)
+    _check(lib().tree_verify_tokens(_ptr(_i32(tok)), _ptr(_i32(parent)), _ptr(_i32(draft)),
+                                    _ptr(None if req_offsets is None else _i32(req_offsets)), n_req, M,
+                                    _ptr(path_len), _ptr(path_nodes), _ptr(bonus), _stream(stream)))
+    return path_len, path_nodes, bonus
+
+
+def tree_verify(logits, parent, draft, req_offsets=None, stream=None):
+    """Greedy acceptance from fp32 logits [M, V]: returns (path_len, path_nodes, bonus)."""
+    if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous float32 CUDA tensor")
+    M, V = logits.shape
+    n_req = 1 if req_offsets is None else req_offsets.numel() - 1
+    path_len, path_nodes, bonus = _tree_out(M, n_req, logits.device)
+    ws = torch.empty(int(lib().tree_verify_workspace_size(M)), dtype=torch.uint8, device=logits.device)
+    _check(lib().tree_verify(_ptr(logits), M, V, _ptr(_i32(parent)), _ptr(_i32(draft)),
+                             _ptr(None if req_offsets is None else _i32(req_offsets)), n_req, _ptr(path_len),
+                             _ptr(path_nodes), _ptr(bonus), _ptr(ws), ws.numel(), _stream(stream)))
+    return path_len, path_nodes, bonus

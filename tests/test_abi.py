@@ -1,0 +1,58 @@
+"""libw12.so builds, loads without a GPU and exports every symbol include/w12.h
+declares; the pure host size queries answer without touching CUDA."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "w12.h")).read()
+    return set(re.findall(r"^W12_API [^(]*?\b(\w+)\(", text, flags=re.M))
+
+
+def test_header_and_binding_agree():
+    import lossless_bit_weights_gb300 as w12
+    names = {n for n, _, _ in w12.SIGNATURES}
+    assert declared_symbols() == names
+
+
+def test_library_exports_every_declared_symbol():
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.w12_abi_version() == 1
+
+
+def test_host_size_queries():
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    assert lib.w12_tile_count(32, 64) == 1
+    assert lib.w12_tile_count(33, 65) == 4
+    assert lib.w12_hi_bytes(5120, 5120) == 160 * 80 * 2048
+    assert lib.w12_lo_bytes(5120, 5120) == 160 * 80 * 1024
+    assert lib.w12_hi_bytes(1, 65536) == -1
+    assert lib.w12_tile_count(0, 5) == -1
+    assert lib.w12_status_string(2) == b"W12_ERR_SHAPE"
+
+
+def test_argument_errors_are_reported_without_device_work():
+    """Null pointers and bad shapes fail host-side checks before any CUDA call."""
+    import ctypes
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    n = ctypes.c_int64(0)
+    assert lib.w12_encode_plan(None, 4, 4, None, None, ctypes.byref(n), None) == 1
+    assert b"null" in lib.w12_last_error()
+    assert lib.w12_encode_plan(ctypes.c_void_p(256), 4, 70000, ctypes.c_void_p(256), ctypes.c_void_p(256),
+                               ctypes.byref(n), None) == 2
+    bad = w12.w12_matrix(0, 5, 256, 256, 256, 256, 0, 0)
+    assert lib.w12_decode(ctypes.byref(bad), ctypes.c_void_p(256), None) == 2
+    good_shape_null_plane = w12.w12_matrix(4, 5, None, 256, 256, 256, 0, 0)
+    assert lib.w12_decode(ctypes.byref(good_shape_null_plane), ctypes.c_void_p(256), None) == 1
+    assert lib.tree_verify_tokens(None, None, None, None, 1, 4, None, None, None, None) == 1
+    p = ctypes.c_void_p(256)
+    assert lib.tree_verify_tokens(p, p, p, None, 2, 4, p, p, p, None) == 1   # several requests need offsets

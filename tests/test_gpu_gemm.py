@@ -1,0 +1,115 @@
+"""GPU W12 / Q8 GEMM against the fp64 oracle: |y - y64| <= 1e-4 * sum|x*w|, and
+repeated calls bit-identical."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import synth
+from tests._gpu_util import assert_gemm_close, device_weights, to_dev16, to_np16
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-4  # tolerance of the verify GEMM, in units of sum_k |x_k * w_k|
+
+
+@pytest.fixture(scope="module")
+def w12():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import lossless_bit_weights_gb300 as m
+    m.lib()
+    return m
+
+
+def check(w12, W, x, q8=False, ws=None):
+    A = w12.encode(to_dev16(W))
+    enc = oracle.encode(W)
+    Wq = oracle.decode_q8(enc) if q8 else oracle.decode(enc)
+    y64, B = oracle.gemm(x, Wq)
+    fn = w12.w12_gemm_q8 if q8 else w12.w12_gemm
+    y = fn(to_dev16(x), A, ws=ws).cpu().numpy()
+    return assert_gemm_close(y, y64, B, REL)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("q8", [False, True])
+def test_tiny_config(w12, M, q8):
+    W = synth.weights(0, 0, 0, 512, 256)
+    x = synth.activations(1, 0, 100, 8, 256)[:M]
+    check(w12, W, x, q8)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 33, 65), (17, 100, 1000), (32, 64, 128), (33, 70, 190),
+                                   (5, 7, 7), (16, 31, 63), (2, 257, 640), (40, 96, 320), (192, 64, 256)])
+@pytest.mark.parametrize("q8", [False, True])
+def test_ragged_shapes(w12, M, N, K, q8):
+    W = synth.weights(0, M, N * 7 + K, N, K)
+    x = synth.activations(1, M, K, M, K)
+    check(w12, W, x, q8)
+
+
+def test_exact_on_small_integers(w12):
+    """Integer-valued weights and activations with small magnitudes: every
+    partial sum is exact in fp32, so the GPU result equals the integer GEMM."""
+    rng = np.random.default_rng(9)
+    M, N, K = 16, 96, 512
+    xi = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    wi = rng.integers(-4, 5, (N, K)).astype(np.float32)
+    bf = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    A = w12.encode(to_dev16(bf(wi)))
+    y = w12.w12_gemm(to_dev16(bf(xi)), A).cpu().numpy()
+    assert np.array_equal(y, xi @ wi.T)
+
+
+def test_deterministic_repeats(w12):
+    W = device_weights(0, 0, 1, 5120, 5120)
+    A = w12.encode(W)
+    x = torch.empty((16, 5120), dtype=torch.int16, device="cuda")
+    synth.activations_dev(1, 0, 1, x)
+    ws = w12.Workspace()
+    ref = w12.w12_gemm(x, A, ws=ws).clone()
+    for _ in range(10):
+        assert torch.equal(w12.w12_gemm(x, A, ws=ws), ref)
+    refq = w12.w12_gemm_q8(x, A, ws=ws).clone()
+    for _ in range(5):
+        assert torch.equal(w12.w12_gemm_q8(x, A, ws=ws), refq)
+
+
+BLOCK = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+
+
+def sampled_block_check(w12, layer, M, q8, n_rows=64, seed_rows=0):
+    """Full-size block at M tokens in the bench's launch configuration; the
+    oracle recomputes a random sample of output channels from host-generated rows."""
+    rng = np.random.default_rng(seed_rows + layer)
+    ws = w12.Workspace()
+    worst = 0.0
+    for tensor, (N, K) in enumerate(BLOCK):
+        Wd = device_weights(0, layer, tensor, N, K)
+        A = w12.encode(Wd)
+        del Wd
+        x_h = synth.activations(1, layer, tensor, M, K)
+        y = (w12.w12_gemm_q8 if q8 else w12.w12_gemm)(to_dev16(x_h), A, ws=ws).cpu().numpy()
+        rows = np.sort(rng.choice(N, n_rows, replace=False))
+        Wr = synth.weight_rows(0, layer, tensor, K, rows)
+        if q8:
+            Wr = oracle.decode_q8(oracle.encode(Wr))
+        y64, B = oracle.gemm(x_h, Wr)
+        worst = max(worst, assert_gemm_close(y[:, rows], y64, B, REL))
+        del A
+        torch.cuda.empty_cache()
+    return worst
+
+
+def test_block_m16_sampled(w12):
+    sampled_block_check(w12, layer=0, M=16, q8=False)
+
+
+def test_block_m32_q8_sampled(w12):
+    sampled_block_check(w12, layer=63, M=32, q8=True)
+
+
+def test_block_m192_sampled(w12):
+    sampled_block_check(w12, layer=1, M=192, q8=False, n_rows=24)
