@@ -51,7 +51,52 @@ def parse_args():
     p.add_argument("--M", type=int, default=16)
     p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead"], default=None,
+                   help="profiling case: repeat one matrix's GEMM (or the LM head) and print its time")
+    p.add_argument("--q8", action="store_true", help="with --only: the 8-bit-view GEMM")
     return p.parse_args()
+
+
+def run_only(args):
+    """One matrix, repeated: the small case ncu captures (one kernel, few launches)."""
+    import torch
+
+    import lossless_bit_weights_gb300 as w12
+    import synth
+
+    torch.cuda.set_device(0)
+    M = args.M
+    if args.only == "lmhead":
+        tensor, (N, K) = 9, LMHEAD
+    else:
+        tensor = [n for n, _, _ in BLOCK].index(args.only)
+        _, N, K = BLOCK[tensor]
+    W = torch.empty((N, K), dtype=torch.int16, device="cuda")
+    synth.weights_dev(0, 0, tensor, W)
+    A = w12.encode(W)
+    del W
+    torch.cuda.empty_cache()
+    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    synth.activations_dev(1, 0, tensor, x)
+    ws = w12.Workspace()
+    if args.only == "lmhead":
+        fn = lambda: w12.w12_lmhead_argmax(x, A, q8=args.q8, ws=ws)
+    else:
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        fn = lambda: (w12.w12_gemm_q8 if args.q8 else w12.w12_gemm)(x, A, y=y, ws=ws)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    sb = A.stream_bytes(q8=args.q8) + 2 * M * K + 4 * M * N
+    print(json.dumps({"only": args.only, "q8": args.q8, "M": M, "N": N, "K": K, "us": us,
+                      "stream_GBps": sb / us / 1e3, "decoded_GBps": 2 * N * K / us / 1e3}), flush=True)
 
 
 def peaks():
@@ -407,6 +452,9 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
 
 def main():
     args = parse_args()
+    if args.only:
+        run_only(args)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

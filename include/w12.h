@@ -38,9 +38,12 @@
  *    bits and reserves the all-ones column), 1 <= M.
  *
  * Device layout of a W12 matrix (what w12_encode writes and the kernels read)
- *  The matrix is cut into tiles of 32 channels x 64 columns: RT = ceil(N/32)
- *  row tiles, KC = ceil(K/64) column chunks, tile index i = rt*KC + kc.  Rows
- *  and columns past N and K hold record 0 and never escape.
+ *  The matrix is cut into tiles of 32 channels x 64 columns.  Channels come
+ *  in row blocks of 128 (RB = ceil(N/128), RT = 4*RB row tiles) and columns in
+ *  KC = ceil(K/64) chunks.  The four row tiles of a block at one chunk are
+ *  adjacent: tile (rt, kc) has index ((rt/4)*KC + kc)*4 + rt%4, so one row
+ *  block's chunk is a single 8 KB run of the hi plane and 4 KB of the lo plane.
+ *  Rows and columns past N and K hold record 0 and never escape.
  *  - hi:  RT*KC tiles of 2048 bytes, the 8-bit front view (r >> 4) of each
  *         weight.  In a tile, channel 8q+g and column 16t+j sit at byte
  *         q*512 + (4g+t)*16 + 4*(j/4) + {0,2,1,3}[j%4].
@@ -51,6 +54,9 @@
  *  - esc_tile_ptr: RT*KC+1 u32, exclusive prefix of escape counts per tile.
  *  - esc: n_esc u32 entries, grouped by tile and sorted by (channel, column)
  *         within a tile: raw bf16 | (column-in-chunk) << 16 | (channel-in-tile) << 22.
+ *         The allocation holds ceil(n_esc/4)*4 entries (at least 4): the GEMM
+ *         copies escapes in aligned 16-byte runs.
+ *  hi, lo and esc must be 16-byte aligned (cudaMalloc gives 256).
  *  w12_export_canonical converts to the canonical planes for comparison.
  */
 #ifndef W12_H
@@ -102,8 +108,8 @@ W12_API int w12_abi_version(void);
 
 /* ---- sizes (pure host functions, no CUDA calls) ------------------------- */
 
-/* Bytes of the hi plane, the lo plane, and tiles (RT*KC) of an N x K matrix;
- * -1 for an invalid shape. */
+/* Bytes of the hi plane, the lo plane, and tiles (4*ceil(N/128)*ceil(K/64)) of
+ * an N x K matrix; -1 for an invalid shape. */
 W12_API int64_t w12_hi_bytes(int64_t N, int64_t K);
 W12_API int64_t w12_lo_bytes(int64_t N, int64_t K);
 W12_API int64_t w12_tile_count(int64_t N, int64_t K);

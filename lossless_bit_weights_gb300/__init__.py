@@ -147,6 +147,12 @@ class W12Matrix:
         return rec + 4 * self.n_esc + 4 * self.esc_tile_ptr.numel() + self.base.numel()
 
 
+def esc_alloc_entries(n_esc: int) -> int:
+    """Entries to allocate for an escape list: a multiple of 4 (the GEMM stages
+    escapes in 16-byte runs), at least 4."""
+    return max(4, (n_esc + 3) // 4 * 4)
+
+
 def tile_count(N: int, K: int) -> int:
     return int(lib().w12_tile_count(N, K))
 
@@ -167,7 +173,7 @@ def encode(W: torch.Tensor, stream=None) -> W12Matrix:
     _check(L.w12_encode_plan(_ptr(W), N, K, _ptr(base), _ptr(tp), ctypes.byref(n_esc), s))
     hi = torch.empty(int(L.w12_hi_bytes(N, K)), dtype=torch.uint8, device=dev)
     lo = torch.empty(int(L.w12_lo_bytes(N, K)), dtype=torch.uint8, device=dev)
-    esc = torch.empty(max(int(n_esc.value), 1), dtype=torch.int32, device=dev)
+    esc = torch.empty(esc_alloc_entries(int(n_esc.value)), dtype=torch.int32, device=dev)
     A = W12Matrix(N, K, hi, lo, base, tp, esc, n_esc.value)
     _check(L.w12_encode(_ptr(W), A.desc(), s))
     return A

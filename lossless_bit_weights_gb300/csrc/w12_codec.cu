@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(256) k_tile_count(const uint16_t* __restrict__
   const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (blockIdx.x == 0 && threadIdx.x == 0) tile_ptr[T] = 0;
   if (tile >= T) return;
-  const int64_t rt = tile / KC, kc = tile % KC;
+  int64_t rt, kc;
+  tile_coords(tile, KC, rt, kc);
   const int64_t n = rt * kTileRows + lane;
   uint32_t v[32];
   load_chunk(W, N, K, vec, n, kc, v);
@@ -178,7 +179,8 @@ __global__ void __launch_bounds__(256) k_pack(const uint16_t* __restrict__ W, in
   const int lane = threadIdx.x & 31;
   const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (tile >= T) return;
-  const int64_t rt = tile / KC, kc = tile % KC;
+  int64_t rt, kc;
+  tile_coords(tile, KC, rt, kc);
   const int64_t n = rt * kTileRows + lane;
   const int64_t k0 = kc * kTileK;
   uint32_t v[32];
@@ -253,7 +255,8 @@ __global__ void __launch_bounds__(256) k_decode(const uint8_t* __restrict__ hi, 
   const int lane = threadIdx.x & 31;
   const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (tile >= T) return;
-  const int64_t rt = tile / KC, kc = tile % KC;
+  int64_t rt, kc;
+  tile_coords(tile, KC, rt, kc);
   const int64_t n = rt * kTileRows + lane;
   const int64_t k0 = kc * kTileK;
   const int q = lane >> 3, g = lane & 7;
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(256) k_decode(const uint8_t* __restrict__ hi, 
       uint2 l = make_uint2(0, 0);
       if (!Q8) l = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
       uint32_t pr[8];
-      decode16<Q8>(h, l, base2, pr);
+      decode16<Q8>(h, l, base2, DecodeMul{16u, 256u, 1u << 28}, pr);
       const int64_t kb = k0 + 16 * t;
       if (vec && kb + 16 <= K) {
         uint4* dst = reinterpret_cast<uint4*>(row + kb);
@@ -298,7 +301,8 @@ __global__ void __launch_bounds__(256) k_export_planes(const uint8_t* __restrict
   const int lane = threadIdx.x & 31;
   const int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (tile >= T) return;
-  const int64_t rt = tile / KC, kc = tile % KC;
+  int64_t rt, kc;
+  tile_coords(tile, KC, rt, kc);
   const int64_t n = rt * kTileRows + lane;
   if (n >= N) return;
   const int64_t lo_row = (K + 1) / 2;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(256) k_export_esc(const uint32_t* __restrict__
   uint32_t off = (pass == 1 && n < N) ? rowptr[n] : 0;
   uint32_t cnt = 0;
   for (int64_t kc = 0; kc < KC; ++kc) {
-    const int64_t tile = rt * KC + kc;
+    const int64_t tile = tile_index(rt, kc, KC);
     const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
     for (uint32_t e = e0; e < e1; ++e) {
       const uint32_t ent = esc[e];

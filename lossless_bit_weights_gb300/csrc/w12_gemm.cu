@@ -1,24 +1,30 @@
-// w12_gemm.cu - decode-fused weight-streaming GEMM for few rows (M <= 32 per
-// launch), its 8-bit-view variant, and the LM-head argmax epilogue.
+// w12_gemm.cu - decode-fused weight-streaming GEMM for few rows (up to 32
+// tokens per launch), its 8-bit-view variant, and the LM-head argmax epilogue.
 //
 // The SpecPilot summary page (onedev.kr/papers/1654), section "What's
 // different", describes a GEMM that decodes the 12-bit records in registers,
 // hides the decode behind the memory stream and stays deterministic with
-// stream-K.  This kernel:
-//  - streams each warp's contiguous run of 32x64 weight tiles (2 KB of the
-//    front-byte plane + 1 KB of nibbles) with 16-byte L1-bypassing loads,
-//    prefetched two tiles ahead;
-//  - decodes 16 weights per thread in registers to bf16 (sign, base+offset,
-//    mantissa: a shift, two masks, one add, one or), stores them to a
-//    swizzled shared tile, and writes the tile's escapes over their slots;
-//  - feeds mma.sync m16n8k16 with the weights as the 16-row A operand
-//    (ldmatrix) and up to 32 tokens as 8-column B blocks ("swap-AB");
-//  - splits the flat list of (row tile, column chunk) iterations evenly over
-//    all warps (stream-K).  A warp that owns only part of a row tile writes
-//    its partial sums to a fixed slot; the last of that tile's warps to
-//    arrive (atomic counter, no waiting) adds the slots in slot order.  The
-//    partition depends only on the shape and the device's warp count, so
-//    repeated calls give identical bits.
+// stream-K.  This kernel is built for sm_103a:
+//  - one CTA = 1 producer warp + 4 consumer warps; a unit of work is a row
+//    block (128 channels = 4 row tiles) x one 64-column chunk;
+//  - the producer fills a 3-stage shared-memory ring with bulk copies (TMA):
+//    the block's 8 KB of front bytes and 4 KB of nibbles (adjacent in the
+//    device tile order), the block's escape run, and the chunk of x through a
+//    2-D tensor map (128-byte swizzle; rows past M and columns past K read as
+//    zero);
+//  - each consumer warp decodes its 32x64 tile in registers to bf16 (sign,
+//    base+offset, mantissa), stores it to a swizzled tile, writes the tile's
+//    escapes over their slots, and runs mma.sync m16n8k16 with the weights as
+//    the 16-row A operand and the tokens as 8-column B blocks (swap-AB), both
+//    through ldmatrix;
+//  - the flat list of (row block, chunk) units is split evenly over CTAs
+//    (stream-K).  A CTA that owns part of a row block writes partial sums to
+//    a fixed slot; the last CTA of that block to arrive (atomic counter, no
+//    waiting) adds the slots in slot order, so results are bit-identical
+//    from call to call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -28,10 +34,28 @@
 namespace w12 {
 namespace {
 
-constexpr int kWarps = 4;                   // warps per block
-constexpr int kWarpSmem = kTileRows * 128;  // decoded 32x64 bf16 tile per warp
-constexpr int kMinIters = 6;                // fewest tile iterations per warp
-constexpr int kMaxTokens = 32;              // tokens per launch
+constexpr int kConsumers = kBlockTiles;          // consumer warps, one row tile each
+constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
+constexpr int kATile = kTileRows * 128;          // decoded 32x64 bf16 tile (swizzled)
+constexpr int kEscRun = 128;                     // escape entries a stage holds
+#ifndef W12_GEMM_STAGES
+#define W12_GEMM_STAGES 3
+#endif
+#ifndef W12_GEMM_PREFETCH
+#define W12_GEMM_PREFETCH 0
+#endif
+#ifndef W12_GEMM_BLOCKS_PER_SM
+#define W12_GEMM_BLOCKS_PER_SM 3
+#endif
+constexpr int kBlocksPerSM = W12_GEMM_BLOCKS_PER_SM;
+#ifdef W12_CONST_MUL
+#define W12_KMUL DecodeMul{16u, 256u, 1u << 28}
+#else
+#define W12_KMUL a.mul
+#endif
+constexpr int kMinIters = 4;                     // fewest units per CTA
+constexpr int kMaxTokens = 32;                   // tokens per launch
+constexpr int kPrefetch = W12_GEMM_PREFETCH;      // units warmed in L2 ahead of the ring
 
 enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1 };
 
@@ -41,179 +65,267 @@ struct GemmArgs {
   const uint8_t* base;
   const uint32_t* tile_ptr;
   const uint32_t* esc;
-  int64_t N, KC, T, W;
-  const uint16_t* x;   // [M][ldx] bf16, ldx even, zero past K
-  int64_t ldx;
-  int M;               // tokens of this launch (<= 8*NB)
-  float* y;            // EPI_STORE: y[m*ldy + n]
+  int64_t N, KC, T, G;  // T = row blocks * KC units, G = CTAs of the partition
+  int M;                // tokens of this launch (<= 8*NB)
+  int tok0;             // first token of this launch (x tensor-map row)
+  float* y;             // EPI_STORE: y[m*ldy + n] (already offset to tok0)
   int64_t ldy;
   unsigned long long* pbest;  // EPI_ARGMAX: pbest[rt*ldp + tok0 + m]
   int64_t ldp;
-  int tok0;
   float* slots;
   uint32_t* counters;
+  uint32_t* error;
+  DecodeMul mul;
 };
 
-struct Stage {
-  uint4 h[4];
-  uint2 l[4];
-  uint32_t ent;
-  uint32_t e0, cnt;
-};
-
-__device__ __forceinline__ int64_t warp_of_iter(int64_t i, int64_t W, int64_t T) { return ((i + 1) * W - 1) / T; }
-
-template <bool Q8>
-__device__ __forceinline__ void issue(Stage& st, const GemmArgs& a, int64_t c, int lane, uint64_t pol,
-                                      uint32_t& tp_cur, uint32_t& tp_nxt) {
-  const uint8_t* hp = a.hi + c * kHiTileBytes + lane * 16;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) st.h[q] = ldg_stream16(hp + q * 512, pol);
-  if (!Q8) {
-    const uint8_t* lp = a.lo + c * kLoTileBytes + lane * 8;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) st.l[q] = ldg_stream8(lp + q * 256, pol);
-  }
-  st.e0 = tp_cur;
-  st.cnt = tp_nxt - tp_cur;
-  st.ent = lane < (int)st.cnt ? __ldg(a.esc + tp_cur + lane) : 0u;
-  tp_cur = tp_nxt;
-  tp_nxt = (c + 2 <= a.T) ? __ldg(a.tile_ptr + c + 2) : tp_nxt;
-}
-
+// Shared-memory plan: [x stages (1 KB aligned)][record stages][A tiles][barriers]
 template <int NB, bool Q8>
-__device__ __forceinline__ void compute(Stage& st, const GemmArgs& a, int64_t c, int64_t kx, int64_t seg_end,
-                                        int lane, uint32_t sm, const uint32_t base2[4], float acc[2][NB][4],
-                                        uint64_t pol, uint32_t& tp_cur, uint32_t& tp_nxt) {
-  const int g = lane >> 2, t = lane & 3;
-  // B fragments (tokens) for the chunk: b0 = x[tok][k 16s+2t..+1], b1 = +8
-  uint32_t bf[4][NB][2];
-#pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    const int tok = nb * 8 + g;
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(a.x + (int64_t)tok * a.ldx + kx) + t;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      bf[s][nb][0] = tok < a.M ? __ldg(xr + 8 * s) : 0u;
-      bf[s][nb][1] = tok < a.M ? __ldg(xr + 8 * s + 4) : 0u;
-    }
-  }
-  // decode the four channel groups this thread holds into the shared tile
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t pr[8];
-    decode16<Q8>(st.h[q], st.l[q], base2[q], pr);
-    const int r = 8 * q + g;
-    const uint32_t row = sm + r * 128;
-    sts128(row + (((2 * t) ^ g) << 4), pr[0], pr[1], pr[2], pr[3]);
-    sts128(row + (((2 * t + 1) ^ g) << 4), pr[4], pr[5], pr[6], pr[7]);
-  }
-  __syncwarp();
-  // escapes overwrite their slots with the exact bf16 value
-  if (lane < (int)st.cnt) {
-    const uint32_t e = st.ent;
-    const int rr = esc_row(e), kk = esc_col(e);
-    sts16(sm + rr * 128 + ((((kk >> 3) ^ (rr & 7))) << 4) + (kk & 7) * 2, (uint16_t)esc_raw(e));
-  }
-  for (uint32_t extra = 32; extra < st.cnt; extra += 32) {
-    if (extra + lane < st.cnt) {
-      const uint32_t e = __ldg(a.esc + st.e0 + extra + lane);
-      const int rr = esc_row(e), kk = esc_col(e);
-      sts16(sm + rr * 128 + ((((kk >> 3) ^ (rr & 7))) << 4) + (kk & 7) * 2, (uint16_t)esc_raw(e));
-    }
-  }
-  __syncwarp();
-  if (c + 2 < seg_end) issue<Q8>(st, a, c + 2, lane, pol, tp_cur, tp_nxt);
-  // tensor-core products: A = weights (ldmatrix), B = tokens
-  const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = 16 * h + (mi & 1) * 8 + rr;
-      const int chunk = 2 * s + (mi >> 1);
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(sm + row * 128 + ((chunk ^ rr) << 4), a0, a1, a2, a3);
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(acc[h][nb], a0, a1, a2, a3, bf[s][nb][0], bf[s][nb][1]);
-    }
-  }
-  __syncwarp();
+struct Plan {
+  static constexpr int kStages = W12_GEMM_STAGES;
+  static constexpr int kX = 8 * NB * 128;                     // swizzled x chunk
+  static constexpr int kHi = kBlockTiles * kHiTileBytes;      // 8 KB
+  static constexpr int kLo = Q8 ? 0 : kBlockTiles * kLoTileBytes;
+  static constexpr int kOffLo = kHi;
+  static constexpr int kOffEsc = kHi + kLo;
+  static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
+  static constexpr int kRec = kOffHdr + 32;
+  static constexpr int kOffRec = kStages * kX;
+  static constexpr int kOffA = kOffRec + kStages * kRec;
+  static constexpr int kOffBar = kOffA + kConsumers * kATile;
+  static constexpr int kBytes = kOffBar + kStages * 16 + 16;
+};
+
+__device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+
+__device__ __forceinline__ void tma_x(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+      "[%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
 
 template <int NB, bool Q8, int EPI>
-__global__ void __launch_bounds__(kWarps * 32, 3) k_gemm(const GemmArgs a) {
-  __shared__ __align__(128) uint8_t smem[kWarps * kWarpSmem];
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemm(const __grid_constant__ CUtensorMap xmap,
+                                                                  const GemmArgs a) {
+  using P = Plan<NB, Q8>;
+  constexpr int S = P::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint32_t last_flag;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
-  if (w >= a.W) return;
-  const uint32_t sm = smem_u32(smem + warp * kWarpSmem);
-  const uint64_t pol = policy_evict_first();
-  const int g = lane >> 2, t = lane & 3;
-  const int64_t it1 = (w + 1) * a.T / a.W;
-  int64_t it = w * a.T / a.W;
+  const int64_t b = blockIdx.x;
+  if (b >= a.G) return;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full0 = sbase + P::kOffBar, empty0 = full0 + 8 * S;
+  const int64_t u0 = b * a.T / a.G, u1 = (b + 1) * a.T / a.G;
+  const int nun = (int)(u1 - u0);
 
-  while (it < it1) {
-    const int64_t rt = it / a.KC;
-    const int64_t kc0 = it - rt * a.KC;
-    const int64_t seg_end = it1 < (rt + 1) * a.KC ? it1 : (rt + 1) * a.KC;
-    uint32_t base2[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t n = rt * kTileRows + 8 * q + g;
-      const uint32_t b = n < a.N ? (uint32_t)__ldg(a.base + n) : 1u;
-      base2[q] = (b << 7) | (b << 23);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumers);
     }
-    float acc[2][NB][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[h][nb][i] = 0.f;
+    mbar_init_fence();
+  }
+  __syncthreads();
 
-    uint32_t tp_cur = __ldg(a.tile_ptr + it), tp_nxt = __ldg(a.tile_ptr + it + 1);
-    Stage sa, sb;
-    issue<Q8>(sa, a, it, lane, pol, tp_cur, tp_nxt);
-    if (it + 1 < seg_end) issue<Q8>(sb, a, it + 1, lane, pol, tp_cur, tp_nxt);
-    for (int64_t c = it; c < seg_end; c += 2) {
-      compute<NB, Q8>(sa, a, c, (c - rt * a.KC) * kTileK, seg_end, lane, sm, base2, acc, pol, tp_cur, tp_nxt);
-      if (c + 1 < seg_end)
-        compute<NB, Q8>(sb, a, c + 1, (c + 1 - rt * a.KC) * kTileK, seg_end, lane, sm, base2, acc, pol, tp_cur,
-                        tp_nxt);
+  if (warp == kConsumers) {
+    // ================================================================ producer
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    int64_t wb = 4 * u0;  // window of tile_ptr[wb .. wb+63] held across the lanes
+    const int64_t TT = 4 * a.T;
+    uint32_t w0 = wb + lane <= TT ? __ldg(a.tile_ptr + wb + lane) : 0u;
+    uint32_t w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
+    int64_t kc = u0 % a.KC;
+    if (kPrefetch > 0 && lane == 0)
+      for (int j = S; j < S + kPrefetch && j < nun; ++j) {
+        prefetch_l2(a.hi + (u0 + j) * P::kHi, P::kHi);
+        if (!Q8) prefetch_l2(a.lo + (u0 + j) * (kBlockTiles * kLoTileBytes), P::kLo);
+      }
+    for (int j = 0; j < nun; ++j) {
+      const int s = j % S;
+      const int64_t u = u0 + j;
+      if (kPrefetch > 0 && lane == 0 && j + S + kPrefetch < nun) {
+        const int64_t up = u + S + kPrefetch;
+        prefetch_l2(a.hi + up * P::kHi, P::kHi);
+        if (!Q8) prefetch_l2(a.lo + up * (kBlockTiles * kLoTileBytes), P::kLo);
+      }
+      if (j >= S && !mbar_wait_bounded(empty0 + 8 * s, (uint32_t)(((j / S) - 1) & 1))) {
+        if (lane == 0) atomicOr(a.error, 1u);
+        return;
+      }
+      if (4 * u - wb >= 32) {
+        w0 = w1;
+        wb += 32;
+        w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
+      }
+      const int d = (int)(4 * u - wb);
+      // lane i < 5 gets tile_ptr[4u + i]
+      const int src = d + (lane < 5 ? lane : 0);
+      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
+      const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
+      const uint32_t tpv = src < 32 ? v0 : v1;
+      const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
+      const uint32_t e0 = t_first & ~3u;
+      uint32_t e1 = (t_last + 3u) & ~3u;
+      if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
+      const uint32_t esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
+      uint8_t* rec = smem + P::kOffRec + s * P::kRec;
+      if (lane < 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = tpv;
+      if (lane == 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[5] = e0;
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t full = full0 + 8 * s;
+        const uint32_t recs = sbase + P::kOffRec + s * P::kRec;
+        mbar_arrive_expect_tx(full, P::kHi + P::kLo + P::kX + esc_bytes);
+        bulk_g2s(recs, a.hi + u * P::kHi, P::kHi, full, pol_w);
+        if (!Q8) bulk_g2s(recs + P::kOffLo, a.lo + u * (kBlockTiles * kLoTileBytes), P::kLo, full, pol_w);
+        if (esc_bytes) bulk_g2s(recs + P::kOffEsc, a.esc + e0, esc_bytes, full, pol_w);
+        tma_x(sbase + s * P::kX, &xmap, (int)(kc * kTileK), a.tok0, full, pol_x);
+      }
+      if (++kc == a.KC) kc = 0;
     }
+    return;
+  }
 
-    // ---- combine partial row tiles (fixed slot order)
-    const bool whole = (kc0 == 0) && (seg_end == (rt + 1) * a.KC);
-    bool emit = true;
-    if (!whole) {
-      const int64_t wf = warp_of_iter(rt * a.KC, a.W, a.T);
-      const int64_t wl = warp_of_iter((rt + 1) * a.KC - 1, a.W, a.T);
-      const int64_t ncov = wl - wf + 1;
-      constexpr int kSlot = 2 * NB * 4 * 32;  // floats per slot
-      float4* slot = reinterpret_cast<float4*>(a.slots + (wf + rt + (w - wf)) * kSlot);
+  // ================================================================ consumers
+  const int w = warp;  // row tile inside the block
+  uint8_t* atp = smem + P::kOffA + w * kATile;
+  const uint32_t at = smem_u32(atp);
+  const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
+  float acc[2][NB][4];
+  uint32_t base2[4];
+  int64_t rb = u0 / a.KC;
+  int64_t kc = u0 - rb * a.KC;
+  int64_t seg_start = u0;
+
+  for (int j = 0; j < nun; ++j) {
+    const int64_t u = u0 + j;
+    const int s = j % S;
+    const uint8_t* rec = smem + P::kOffRec + s * P::kRec;
+    if (j == 0 || kc == 0) {  // a new row block starts
+      seg_start = u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t n = (rb * kBlockTiles + w) * kTileRows + 8 * q + g;
+        const uint32_t bb = n < a.N ? (uint32_t)__ldg(a.base + n) : 1u;
+        base2[q] = (bb << 7) | (bb << 23);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
-          slot[(h * NB + nb) * 32 + lane] = make_float4(acc[h][nb][0], acc[h][nb][1], acc[h][nb][2], acc[h][nb][3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[h][nb][i] = 0.f;
+    }
+    if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)((j / S) & 1))) {
+      if (lane == 0) atomicOr(a.error, 2u);
+      return;
+    }
+    // ---- decode this warp's tile into its swizzled A tile
+    uint4 hq[4];
+    uint2 lq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hq[q] = *reinterpret_cast<const uint4*>(rec + w * kHiTileBytes + q * 512 + lane * 16);
+      lq[q] = Q8 ? make_uint2(0u, 0u)
+                 : *reinterpret_cast<const uint2*>(rec + P::kOffLo + w * kLoTileBytes + q * 256 + lane * 8);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t pr[8];
+      decode16<Q8>(hq[q], lq[q], base2[q], W12_KMUL, pr);
+      uint8_t* row = atp + (8 * q + g) * 128;
+      *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+    }
+    __syncwarp();
+    // ---- this tile's escapes overwrite their slots with the exact value
+    {
+      const uint32_t* hdr = reinterpret_cast<const uint32_t*>(rec + P::kOffHdr);
+      const uint32_t ta = hdr[w], tb = hdr[w + 1], e0 = hdr[5];
+      const uint32_t* run = reinterpret_cast<const uint32_t*>(rec + P::kOffEsc);
+      for (uint32_t e = ta + lane; e < tb; e += 32) {
+        const uint32_t ent = e - e0 < (uint32_t)kEscRun ? run[e - e0] : __ldg(a.esc + e);
+        const int er = esc_row(ent), ek = esc_col(ent);
+        *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
+            (uint16_t)esc_raw(ent);
+      }
+    }
+    __syncwarp();
+    // ---- tensor-core products: A = weights, B = tokens (ldmatrix on both)
+    const uint32_t xs = sbase + s * P::kX;
+#pragma unroll
+    for (int k16 = 0; k16 < 4; ++k16) {
+      uint32_t bfr[NB][2];
+      if (NB == 1) {
+        ldsm_x2(xs + rr * 128 + (((2 * k16 + (mi & 1)) ^ rr) << 4), bfr[0][0], bfr[0][1]);
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < NB; nb += 2) {
+          const int tok = (nb + (mi >> 1)) * 8 + rr;
+          ldsm_x4(xs + tok * 128 + (((2 * k16 + (mi & 1)) ^ rr) << 4), bfr[nb][0], bfr[nb][1], bfr[nb + 1][0],
+                  bfr[nb + 1][1]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = 16 * h + (mi & 1) * 8 + rr;
+        const int chunk = 2 * k16 + (mi >> 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(at + row * 128 + ((chunk ^ rr) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(acc[h][nb], a0, a1, a2, a3, bfr[nb][0], bfr[nb][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive(empty0 + 8 * s);
+    }
+    const bool block_end = (kc + 1 == a.KC);
+    const bool range_end = (j + 1 == nun);
+    if (++kc == a.KC) kc = 0;
+    if (!block_end && !range_end) continue;
+
+    // ---- row block finished (or this CTA's share of it): combine in slot order
+    const bool whole = (seg_start == rb * a.KC) && block_end;
+    bool emit = true;
+    if (!whole) {
+      const int64_t cf = cta_of_unit(rb * a.KC, a.G, a.T);
+      const int64_t cl = cta_of_unit((rb + 1) * a.KC - 1, a.G, a.T);
+      const int64_t ncov = cl - cf + 1;
+      constexpr int kWarpSlot = 2 * NB * 4 * 32;  // floats per warp in a slot
+      float4* slot = reinterpret_cast<float4*>(a.slots + ((cf + rb + (b - cf)) * kConsumers + w) * kWarpSlot);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+          __stcg(slot + (h * NB + nb) * 32 + lane,
+                 make_float4(acc[h][nb][0], acc[h][nb][1], acc[h][nb][2], acc[h][nb][3]));
       __threadfence();
-      __syncwarp();
-      uint32_t old = 0;
-      if (lane == 0) old = atomicAdd(a.counters + rt, 1u);
-      old = __shfl_sync(0xFFFFFFFFu, old, 0);
-      emit = (int64_t)old == ncov - 1;
+      consumers_sync();
+      if (threadIdx.x == 0) last_flag = atomicAdd(a.counters + rb, 1u);
+      consumers_sync();
+      emit = (int64_t)last_flag == ncov - 1;
+      consumers_sync();
       if (emit) {
         __threadfence();
-        if (lane == 0) a.counters[rt] = 0u;
+        if (threadIdx.x == 0) a.counters[rb] = 0u;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[h][nb][i] = 0.f;
-        for (int64_t j = 0; j < ncov; ++j) {
-          const float4* sj = reinterpret_cast<const float4*>(a.slots + (wf + rt + j) * kSlot);
+        for (int64_t jj = 0; jj < ncov; ++jj) {
+          const float4* sj = reinterpret_cast<const float4*>(a.slots + ((cf + rb + jj) * kConsumers + w) * kWarpSlot);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -227,8 +339,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_gemm(const GemmArgs a) {
         }
       }
     }
-
     if (emit) {
+      const int64_t rt = rb * kBlockTiles + w;
       if (EPI == EPI_STORE) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -246,7 +358,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_gemm(const GemmArgs a) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             unsigned long long best = 0ull;
-            // rows in increasing order: g, g+8, g+16, g+24
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -269,11 +380,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) k_gemm(const GemmArgs a) {
           }
       }
     }
-    it = seg_end;
+    if (block_end) ++rb;
   }
 }
 
-// Zero-padded copy of x: xp[m][ldx] with ldx = KC*64.
+// Copy of x with row pitch ldx (a multiple of 8 elements), zero past K.
 __global__ void k_pad_x(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint16_t* __restrict__ xp) {
   const int64_t total = M * ldx;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -326,29 +437,31 @@ int device_sms(int* sms) {
   return W12_OK;
 }
 
-// Warps of the stream-K partition for a T-iteration problem.
-int64_t partition_warps(int64_t T, int sms) {
-  const int64_t resident = (int64_t)sms * 3 * kWarps;  // 3 blocks of kWarps per SM (launch bounds)
-  int64_t w = (T + kMinIters - 1) / kMinIters;
-  return std::max<int64_t>(1, std::min(w, resident));
+// CTAs of the stream-K partition for a T-unit problem.
+int64_t partition_ctas(int64_t T, int sms) {
+  const int64_t resident = (int64_t)sms * kBlocksPerSM;
+  const int64_t g = (T + kMinIters - 1) / kMinIters;
+  return std::max<int64_t>(1, std::min(g, resident));
 }
 
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t counters, slots, xpad, pbest, total;
+  size_t counters, error, slots, xpad, pbest, total;
 };
 
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
-  const int64_t RT = row_tiles(N), KC = k_chunks(K), T = RT * KC;
-  const int64_t W = partition_warps(T, sms);
+  const int64_t RB = row_blocks(N), RT = row_tiles(N), KC = k_chunks(K), T = RB * KC;
+  const int64_t G = partition_ctas(T, sms);
   const int64_t Mg = std::min<int64_t>(M, kMaxTokens);
   const int64_t nb = Mg <= 8 ? 1 : Mg <= 16 ? 2 : 4;
   WsLayout L{};
   L.counters = 0;
-  size_t off = align256((size_t)RT * 4);
+  size_t off = align256((size_t)RB * 4);
+  L.error = off;
+  off += 256;
   L.slots = off;
-  off = align256(off + (size_t)(RT + W) * (size_t)(2 * nb * 4 * 32) * 4);
+  off = align256(off + (size_t)(RB + G) * kConsumers * (size_t)(2 * nb * 4 * 32) * 4);
   L.xpad = off;
   off = align256(off + (size_t)M * (size_t)(KC * kTileK) * 2);
   L.pbest = off;
@@ -357,20 +470,55 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   return L;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over x[M][ldx] bf16: box of 64 columns x rows tokens, 128-byte swizzle.
+int make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(W12_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(W12_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return W12_OK;
+}
+
 template <int NB, bool Q8, int EPI>
-int launch_one(const GemmArgs& a, cudaStream_t s) {
-  const unsigned blocks = (unsigned)((a.W + kWarps - 1) / kWarps);
-  k_gemm<NB, Q8, EPI><<<blocks, kWarps * 32, 0, s>>>(a);
+int launch_one(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  constexpr int smem = Plan<NB, Q8>::kBytes;
+  static int configured_for_device[64] = {0};
+  int dev = 0;
+  W12_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= 64 || !configured_for_device[dev]) {
+    W12_CUDA_TRY(cudaFuncSetAttribute(k_gemm<NB, Q8, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    if (dev < 64) configured_for_device[dev] = 1;
+  }
+  k_gemm<NB, Q8, EPI><<<(unsigned)a.G, kThreads, smem, s>>>(map, a);
   W12_LAUNCH_CHECK("w12 gemm kernel");
   return W12_OK;
 }
 
 template <bool Q8, int EPI>
-int launch_nb(int nb, const GemmArgs& a, cudaStream_t s) {
+int launch_nb(int nb, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   switch (nb) {
-    case 1: return launch_one<1, Q8, EPI>(a, s);
-    case 2: return launch_one<2, Q8, EPI>(a, s);
-    default: return launch_one<4, Q8, EPI>(a, s);
+    case 1: return launch_one<1, Q8, EPI>(map, a, s);
+    case 2: return launch_one<2, Q8, EPI>(map, a, s);
+    default: return launch_one<4, Q8, EPI>(map, a, s);
   }
 }
 
@@ -381,18 +529,20 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   if (!x || (!argmax && !y) || (argmax && !tok)) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
   if (!ws) return fail(W12_ERR_INVALID_ARG, "%s: null workspace", fn);
+  if ((((uintptr_t)A->hi | (uintptr_t)A->lo | (uintptr_t)A->esc) & 15u) != 0)
+    return fail(W12_ERR_INVALID_ARG, "%s: hi, lo and esc must be 16-byte aligned", fn);
   int sms = 0;
   if ((st = device_sms(&sms))) return st;
   const WsLayout L = ws_layout(M, A->N, A->K, argmax, sms);
   if (ws_bytes < L.total)
     return fail(W12_ERR_BUFFER_TOO_SMALL, "%s: workspace %zu bytes < %zu required", fn, ws_bytes, L.total);
-  const int64_t RT = row_tiles(A->N), KC = k_chunks(A->K), T = RT * KC;
+  const int64_t RB = row_blocks(A->N), RT = row_tiles(A->N), KC = k_chunks(A->K), T = RB * KC;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
+  // x through a tensor map needs a 16-byte aligned base and a row pitch that is a multiple of 16 bytes
   const uint16_t* xs = x;
   int64_t ldx = A->K;
-  const bool direct = (A->K % kTileK == 0) && (((uintptr_t)x & 3u) == 0);
-  if (!direct) {
+  if ((A->K % 8) != 0 || ((uintptr_t)x & 15u) != 0) {
     ldx = KC * kTileK;
     uint16_t* xp = reinterpret_cast<uint16_t*>(wsb + L.xpad);
     const int64_t total = M * ldx;
@@ -411,24 +561,27 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.N = A->N;
   a.KC = KC;
   a.T = T;
-  a.W = partition_warps(T, sms);
-  a.ldx = ldx;
+  a.G = partition_ctas(T, sms);
   a.ldy = A->N;
   a.slots = reinterpret_cast<float*>(wsb + L.slots);
   a.counters = reinterpret_cast<uint32_t*>(wsb + L.counters);
+  a.error = reinterpret_cast<uint32_t*>(wsb + L.error);
   a.pbest = reinterpret_cast<unsigned long long*>(wsb + L.pbest);
   a.ldp = M;
+  a.mul = DecodeMul{16u, 256u, 1u << 28};
+  const int64_t Mg0 = std::min<int64_t>(M, kMaxTokens);
+  const int nb = Mg0 <= 8 ? 1 : Mg0 <= 16 ? 2 : 4;
+  CUtensorMap map;
+  if ((st = make_x_map(&map, xs, M, A->K, ldx, 8 * nb))) return st;
   for (int64_t m0 = 0; m0 < M; m0 += kMaxTokens) {
     const int Mg = (int)std::min<int64_t>(kMaxTokens, M - m0);
-    const int nb = Mg <= 8 ? 1 : Mg <= 16 ? 2 : 4;
-    a.x = xs + m0 * ldx;
     a.M = Mg;
     a.tok0 = (int)m0;
     if (!argmax) {
       a.y = y + m0 * A->N;
-      st = q8 ? launch_nb<true, EPI_STORE>(nb, a, s) : launch_nb<false, EPI_STORE>(nb, a, s);
+      st = q8 ? launch_nb<true, EPI_STORE>(nb, map, a, s) : launch_nb<false, EPI_STORE>(nb, map, a, s);
     } else {
-      st = q8 ? launch_nb<true, EPI_ARGMAX>(nb, a, s) : launch_nb<false, EPI_ARGMAX>(nb, a, s);
+      st = q8 ? launch_nb<true, EPI_ARGMAX>(nb, map, a, s) : launch_nb<false, EPI_ARGMAX>(nb, map, a, s);
     }
     if (st) return st;
   }
@@ -459,7 +612,7 @@ using namespace w12;
 
 extern "C" {
 
-size_t w12_gemm_counter_bytes(int64_t N) { return N >= 1 ? align256((size_t)row_tiles(N) * 4) : 0; }
+size_t w12_gemm_counter_bytes(int64_t N) { return N >= 1 ? align256((size_t)row_blocks(N) * 4) : 0; }
 
 size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || N < 1 || K < 1 || K > kMaxK) return 0;

@@ -14,12 +14,27 @@ namespace w12 {
 
 constexpr int kTileRows = 32;        // channels per tile
 constexpr int kTileK = 64;           // columns per tile
+constexpr int kBlockTiles = 4;       // row tiles per row block (128 channels)
 constexpr int kHiTileBytes = 2048;   // 32 x 64 bytes
 constexpr int kLoTileBytes = 1024;   // 32 x 64 nibbles
 constexpr int64_t kMaxK = 65535;
 
-__host__ __device__ inline int64_t row_tiles(int64_t N) { return (N + kTileRows - 1) / kTileRows; }
+// Row blocks of 128 channels; row tiles (4 per block, the last block padded).
+__host__ __device__ inline int64_t row_blocks(int64_t N) { return (N + kTileRows * kBlockTiles - 1) / (kTileRows * kBlockTiles); }
+__host__ __device__ inline int64_t row_tiles(int64_t N) { return row_blocks(N) * kBlockTiles; }
 __host__ __device__ inline int64_t k_chunks(int64_t K) { return (K + kTileK - 1) / kTileK; }
+
+// Tile order: the four row tiles of a row block at one column chunk are
+// adjacent, so tile (rt, kc) has index ((rt/4)*KC + kc)*4 + rt%4.
+__host__ __device__ inline int64_t tile_index(int64_t rt, int64_t kc, int64_t KC) {
+  return ((rt >> 2) * KC + kc) * kBlockTiles + (rt & 3);
+}
+__host__ __device__ inline void tile_coords(int64_t i, int64_t KC, int64_t& rt, int64_t& kc) {
+  const int64_t bk = i >> 2;
+  const int64_t rb = bk / KC;
+  kc = bk - rb * KC;
+  rt = rb * kBlockTiles + (i & 3);
+}
 
 // Byte offset inside a hi tile of channel r (0..31) and column kk (0..63).
 __host__ __device__ inline int hi_offset(int r, int kk) {
@@ -68,21 +83,46 @@ int check_matrix(const w12_matrix* A, bool need_lo, const char* fn);
 // slice) into 8 bf16 pairs in column order: out[p] holds columns 2p (low half)
 // and 2p+1 (high half).  base2 = base<<7 | base<<23.  With Q8 the low nibbles
 // read as zero.
+//
+// Word H_s of the hi slice holds the front bytes of columns 4s, 4s+2, 4s+1,
+// 4s+3 (bytes 0..3), so bytes 0,2 give pair 2s and bytes 1,3 give pair 2s+1.
+// A lane's bf16 is s<<15 | (base + eo)<<7 | m6..4<<4 | m3..0 from a front byte
+// f = s<<7 | eo<<3 | m6..4 and a nibble.  The byte spreading runs on the
+// multiply-add pipe (integer multiplies by 16, 256 and 2^28 as shifts), which
+// leaves the logic pipe with two masks and one merge per pair.
+__device__ __forceinline__ uint32_t mul_hi_add(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// The multipliers come in as run-time values (16, 256, 2^28) so that the
+// compiler keeps them as integer multiply-adds instead of logic-pipe shifts.
+struct DecodeMul {
+  uint32_t m16, m256, m2p28;
+};
+
 template <bool Q8>
-__device__ __forceinline__ void decode16(uint4 h, uint2 l, uint32_t base2, uint32_t out[8]) {
+__device__ __forceinline__ void decode16(uint4 h, uint2 l, uint32_t base2, const DecodeMul& k, uint32_t out[8]) {
   const uint32_t H[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint32_t Hs = H[p >> 1];
-    const uint32_t Q = (p & 1) ? Hs : (Hs << 8);      // front bytes at bits 8..15 / 24..31
-    const uint32_t R = (Q >> 4) & 0x07F007F0u;          // exponent offset and mantissa 6..4
-    const uint32_t S = Q & 0x80008000u;                 // sign
-    uint32_t v = R + S + base2;                         // exponent = base + offset
+  for (int s = 0; s < 4; ++s) {
+    const uint32_t Hs = H[s];
+    const uint32_t L = (s < 2) ? l.x : l.y;
+    // pair 2s: bytes 0 and 2 -> (f & 0x7F) * 16 + base<<7, then sign * 256
+    const uint32_t e7 = Hs & 0x007F007Fu;
+    const uint32_t es = Hs & 0x00800080u;
+    uint32_t ve = es * k.m256 + (e7 * k.m16 + base2);
+    // pair 2s+1: bytes 1 and 3 -> ((f & 0x7F) << 8) >> 4 via the high product, sign already at bit 15
+    const uint32_t o7 = Hs & 0x7F007F00u;
+    uint32_t vo = mul_hi_add(o7, k.m2p28, base2) | (Hs & 0x80008000u);
     if (!Q8) {
-      const uint32_t L = (p < 4) ? l.x : l.y;
-      v |= (L >> (4 * (p & 3))) & 0x000F000Fu;          // mantissa 3..0
+      const int p = 2 * s;  // nibble positions 4*(p&3) and 4*((p+1)&3)
+      ve |= (L >> (4 * (p & 3))) & 0x000F000Fu;
+      vo |= (L >> (4 * ((p + 1) & 3))) & 0x000F000Fu;
     }
-    out[p] = v;
+    out[2 * s] = ve;
+    out[2 * s + 1] = vo;
   }
 }
 
@@ -134,6 +174,82 @@ __device__ __forceinline__ void mma_bf16_16816(float c[4], uint32_t a0, uint32_t
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- mbarrier / bulk-copy (TMA) helpers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the barrier phase with a clock limit (about 2^31 cycles, ~1 s);
+// returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > (1ll << 31)) return false;
+  }
+  return true;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (size multiple of 16, both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Warm L2 with a global range (size multiple of 16, 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& a0, uint32_t& a1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(a0), "=r"(a1) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // Total order used by every argmax: larger key = larger value; NaN lowest;

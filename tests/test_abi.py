@@ -30,8 +30,8 @@ def test_library_exports_every_declared_symbol():
 def test_host_size_queries():
     import lossless_bit_weights_gb300 as w12
     lib = w12.lib()
-    assert lib.w12_tile_count(32, 64) == 1
-    assert lib.w12_tile_count(33, 65) == 4
+    assert lib.w12_tile_count(32, 64) == 4       # one row block of 4 row tiles
+    assert lib.w12_tile_count(129, 65) == 16     # two row blocks, two chunks
     assert lib.w12_hi_bytes(5120, 5120) == 160 * 80 * 2048
     assert lib.w12_lo_bytes(5120, 5120) == 160 * 80 * 1024
     assert lib.w12_hi_bytes(1, 65536) == -1
