@@ -162,6 +162,27 @@ W12_API int w12_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y
 W12_API int w12_gemm_q8(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* ---- verify GEMM without a caller workspace ------------------------------
+ * Not part of the method: the pages have no counterpart.  It is w12_gemm for
+ * callers that cannot give the library a workspace: an engine whose memory
+ * planner has already reserved the whole device, a plugin or callback
+ * interface with no workspace argument, or a latency-critical loop that must
+ * not call cudaMalloc (which can synchronise the device).
+ *  - Scratch is one library-owned device array of w12_gemm_noalloc_max_scratch()
+ *    bytes (16 MiB).  Every GPU that loads libw12.so holds it until the process
+ *    exits.  Nothing is allocated per call.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current.  Make that first call before any stream capture.
+ *  - Each call clears the array's counters on `stream` before the GEMM.
+ *  - All calls share the one array: calls that can overlap on the GPU (other
+ *    streams, other host threads on the same device) race and corrupt each
+ *    other's results.  Serialise them.
+ *  - Shapes needing more scratch than the array holds fail with W12_ERR_SHAPE
+ *    (for example M <= 32 covers N up to ~34K at K = 5120; larger M or N needs
+ *    w12_gemm).  Same result as w12_gemm otherwise.  Asynchronous. */
+W12_API size_t w12_gemm_noalloc_max_scratch(void);
+W12_API int w12_gemm_noalloc(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* stream);
+
 /* ---- LM head with fused argmax ----------------------------------------- */
 
 /* Workspace bytes for the LM-head calls (same counter rule as w12_gemm). */

@@ -59,6 +59,8 @@ SIGNATURES = [
     ("w12_gemm_counter_bytes", _SZ, [_I64]),
     ("w12_gemm", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
     ("w12_gemm_q8", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_gemm_noalloc_max_scratch", _SZ, []),
+    ("w12_gemm_noalloc", ctypes.c_int, [_P, _I64, _MP, _P, _P]),
     ("w12_lmhead_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w12_lmhead_argmax", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
     ("w12_lmhead_argmax_q8", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
@@ -246,6 +248,15 @@ def w12_gemm_q8(x: torch.Tensor, A: W12Matrix, y: torch.Tensor | None = None, ws
                 stream=None) -> torch.Tensor:
     """Same with the 8-bit view of the weights (Q pass)."""
     return _gemm(lib().w12_gemm_q8, x, A, y, ws, stream)
+
+
+def w12_gemm_noalloc(x: torch.Tensor, A: W12Matrix, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """w12_gemm using the library's own fixed scratch instead of a workspace (see include/w12.h)."""
+    x = _bits16(x)
+    M = x.shape[0]
+    y = torch.empty((M, A.N), dtype=torch.float32, device=x.device) if y is None else y
+    _check(lib().w12_gemm_noalloc(_ptr(x), M, A.desc(), _ptr(y), _stream(stream)))
+    return y
 
 
 def w12_lmhead_argmax(x: torch.Tensor, head: W12Matrix, q8: bool = False, tok: torch.Tensor | None = None,

@@ -646,3 +646,69 @@ int w12_lmhead_argmax_q8(const uint16_t* x, int64_t M, const w12_matrix* head, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// w12_gemm without a caller workspace.
+//
+// Some callers cannot give this library a workspace: an inference engine
+// whose memory planner has already handed out the whole device, a plugin or
+// callback interface whose signature has no workspace argument, or a
+// latency-critical loop that must not call cudaMalloc (it can synchronise the
+// device).  For them the GEMM's scratch (stream-K tile counters, the error
+// word, partial-sum slots and, for unaligned x, a padded copy of x) lives in
+// one file-scope device array.  Every GPU that loads the library keeps this
+// array until the process exits.  The array's name is only a host-side stand-in;
+// its device address comes from cudaGetSymbolAddress, looked up once per
+// device with that device current, on the first call.
+namespace w12 {
+
+constexpr size_t kFixedScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
+
+static int fixed_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "w12_gemm_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(W12_ERR_INVALID_ARG, "w12_gemm_noalloc: device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "w12_gemm_noalloc: cudaGetSymbolAddress");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return W12_OK;
+}
+
+}  // namespace w12
+
+extern "C" {
+
+size_t w12_gemm_noalloc_max_scratch(void) { return w12::kFixedScratchBytes; }
+
+int w12_gemm_noalloc(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* stream) {
+  using namespace w12;
+  const char* fn = "w12_gemm_noalloc";
+  int st = check_matrix(A, true, fn);
+  if (st) return st;
+  if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
+  int sms = 0;
+  if ((st = device_sms(&sms))) return st;
+  const WsLayout L = ws_layout(M, A->N, A->K, false, sms);
+  if (L.total > kFixedScratchBytes)
+    return fail(W12_ERR_SHAPE,
+                "%s: M=%lld N=%lld K=%lld needs %zu bytes of scratch; the fixed scratch holds %zu "
+                "(use w12_gemm with a workspace)",
+                fn, (long long)M, (long long)A->N, (long long)A->K, L.total, kFixedScratchBytes);
+  void* scratch = nullptr;
+  if ((st = fixed_scratch_address(&scratch))) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the tile counters and the error word must start at zero on every call
+  W12_CUDA_TRY(cudaMemsetAsync(scratch, 0, L.slots, s));
+  return run_gemm(x, M, A, y, nullptr, false, false, scratch, kFixedScratchBytes, s, fn);
+}
+
+}  // extern "C"
