@@ -138,10 +138,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemm(const __grid_co
   if (warp == kConsumers) {
     // ================================================================ producer
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    int64_t wb = 4 * u0;  // window of tile_ptr[wb .. wb+63] held across the lanes
+    // tile_ptr[wb .. wb+95] held across the lanes in three registers; the third
+    // is loaded 8 units before any shuffle reads it, so the loop never waits on it.
+    int64_t wb = 4 * u0;
     const int64_t TT = 4 * a.T;
     uint32_t w0 = wb + lane <= TT ? __ldg(a.tile_ptr + wb + lane) : 0u;
     uint32_t w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
+    uint32_t w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
     int64_t kc = u0 % a.KC;
     if (kPrefetch > 0 && lane == 0)
       for (int j = S; j < S + kPrefetch && j < nun; ++j) {
@@ -162,8 +165,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemm(const __grid_co
       }
       if (4 * u - wb >= 32) {
         w0 = w1;
+        w1 = w2;
         wb += 32;
-        w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
+        w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
       }
       const int d = (int)(4 * u - wb);
       // lane i < 5 gets tile_ptr[4u + i]

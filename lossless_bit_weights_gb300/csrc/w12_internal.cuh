@@ -198,12 +198,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+#ifndef W12_NAP_NS
+#define W12_NAP_NS 32
+#endif
 // Waits for the barrier phase with a clock limit (about 2^31 cycles, ~1 s);
-// returns false when the limit ran out.
+// returns false when the limit ran out.  It polls with test_wait (which never
+// blocks) and naps a few tens of ns between polls: a thread suspended inside
+// try_wait was measured to notice a completed phase up to ~0.8 us late, while
+// a napping warp still leaves its scheduler's issue slots to the others.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (W12_NAP_NS < 0) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+      if (clock64() - start > (1ll << 31)) return false;
+    }
+    return true;
+  }
+  if (mbar_test_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_test_wait(bar, parity)) {
+    if (W12_NAP_NS > 0) __nanosleep(W12_NAP_NS);
     if (clock64() - start > (1ll << 31)) return false;
   }
   return true;
