@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256) k_decode(const uint8_t* __restrict__ hi, 
       uint2 l = make_uint2(0, 0);
       if (!Q8) l = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
       uint32_t pr[8];
-      decode16<Q8>(h, l, base2, DecodeMul{16u, 256u, 1u << 28}, pr);
+      decode16<Q8>(h, l, base2, W12_DECODE_MUL, pr);
       const int64_t kb = k0 + 16 * t;
       if (vec && kb + 16 <= K) {
         uint4* dst = reinterpret_cast<uint4*>(row + kb);

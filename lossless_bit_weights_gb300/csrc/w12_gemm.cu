@@ -49,7 +49,7 @@ constexpr int kEscRun = 128;                     // escape entries a stage holds
 #endif
 constexpr int kBlocksPerSM = W12_GEMM_BLOCKS_PER_SM;
 #ifdef W12_CONST_MUL
-#define W12_KMUL DecodeMul{16u, 256u, 1u << 28}
+#define W12_KMUL W12_DECODE_MUL
 #else
 #define W12_KMUL a.mul
 #endif
@@ -388,6 +388,517 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemm(const __grid_co
   }
 }
 
+// ===========================================================================
+// tcgen05 variant: decode warps unpack into shared memory; one thread issues
+// the MMAs (5th-generation tensor core, fp32 accumulator in tensor memory).
+//   warps 0..7   decode, two groups of four: group g takes the units j with
+//                j % 2 == g, warp w of a group the row tile w % 4 (32 rows).
+//                The group that decodes a row block's last unit drains the
+//                accumulator (warp w reads TMEM lanes 32(w%4)..32(w%4)+31).
+//   warp 8       TMA producer of the weight records (hi, lo, escape run)
+//   warp 9       lane 0 issues tcgen05.mma (M=128 channels, N=NT tokens, K=16)
+//   warp 10      lane 0 streams x through the tensor map on its own ring
+// A record stage goes back to the producer as soon as its group holds the
+// unit in registers; x stages and A buffers go back on the MMA commit.
+constexpr int kTcGroups = 2;
+constexpr int kTcDecoders = kTcGroups * kBlockTiles;
+constexpr int kTcProducer = kTcDecoders, kTcMma = kTcDecoders + 1, kTcX = kTcDecoders + 2;
+constexpr int kTcThreads = (kTcDecoders + 3) * 32;
+constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 block (16 KB, swizzled)
+
+#ifndef W12_TC_SMALL_BPSM
+#define W12_TC_SMALL_BPSM 2
+#endif
+#ifndef W12_TC_MAX_STAGES
+#define W12_TC_MAX_STAGES 16
+#endif
+
+template <int NT, bool Q8>
+struct TcPlan {
+  static constexpr int kBlocksPerSM = NT <= 32 ? W12_TC_SMALL_BPSM : 1;
+  static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
+  static constexpr int kXStages = NT <= 64 ? 4 : 2;
+  static constexpr int kHi = kBlockTiles * kHiTileBytes;
+  static constexpr int kLo = Q8 ? 0 : kBlockTiles * kLoTileBytes;
+  static constexpr int kOffLo = kHi;
+  static constexpr int kOffEsc = kHi + kLo;
+  static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
+  static constexpr int kRec = kOffHdr + 32;
+  static constexpr int kOffA = kXStages * kX;                 // one A buffer per decode group
+  static constexpr int kOffRec = kOffA + kTcGroups * kABuf;
+  static constexpr int kBudget = (kBlocksPerSM == 2 ? 112 : 224) * 1024;
+  static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 16) / kRec;
+  static constexpr int kStages = kStagesRaw > W12_TC_MAX_STAGES ? W12_TC_MAX_STAGES : kStagesRaw;
+  static constexpr int kOffBar = kOffRec + kStages * kRec;
+  // rec_full[S] rec_empty[S] x_full[SX] x_empty[SX] a_full[2] a_empty[2] epi[2] acc_full acc_empty mma_done
+  static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kTcGroups + 3;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+  static_assert(kStages >= 3, "record ring too shallow");
+  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
+};
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128.
+template <int NT>
+__device__ __forceinline__ constexpr uint32_t umma_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 16 fp32 columns of the accumulator (this warp's lane quarter).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  // the registers are operands of the wait, so no use of them is scheduled before it
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded barrier wait whose outcome is the same in every lane of the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity));
+}
+
+// Rendezvous of a decode group's four warps on an mbarrier, bounded.
+__device__ __forceinline__ bool epi_sync(uint32_t bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = warp_wait(bar, phase & 1u);
+  ++phase;
+  return ok;
+}
+
+// Output of 16 token columns [c0, c0+16) for this warp's 32 rows (row tile rt).
+template <int EPI>
+__device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lane, int c0, const float v[16]) {
+  const int64_t n = rt * kTileRows + lane;
+  if (EPI == EPI_STORE) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = c0 + i;
+      if (tok < a.M && n < a.N) a.y[(int64_t)tok * a.ldy + n] = v[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = c0 + i;
+      unsigned long long best = 0ull;
+      if (n < a.N) {
+        const uint32_t key = (uint32_t)order_key(v[i]) ^ 0x80000000u;
+        best = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+      }
+      if (lane == 0 && tok < a.M) a.pbest[rt * a.ldp + a.tok0 + tok] = best;
+    }
+  }
+}
+
+template <int NT, bool Q8, int EPI>
+__global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
+    k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
+  using P = TcPlan<NT, Q8>;
+  constexpr int S = P::kStages, SX = P::kXStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = blockIdx.x;
+  if (b >= a.G) return;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + P::kOffBar;
+  const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S, x_full0 = bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
+  const uint32_t a_full0 = x_empty0 + 8 * SX, a_empty0 = a_full0 + 8 * kTcGroups, epi0 = a_empty0 + 8 * kTcGroups;
+  const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);  // [0] TMEM address, [1+g] stream-K flag
+  const int64_t u0 = b * a.T / a.G, u1 = (b + 1) * a.T / a.G;
+  const int nun = (int)(u1 - u0);
+
+  // The next kernel on the stream may start as this one's CTAs retire (programmatic
+  // dependent launch): its weight stream does not depend on this kernel's output.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(rec_full0 + 8 * i, 1);
+      mbar_init(rec_empty0 + 8 * i, kBlockTiles);
+    }
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(x_full0 + 8 * i, 1);
+      mbar_init(x_empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < kTcGroups; ++i) {
+      mbar_init(a_full0 + 8 * i, kBlockTiles);
+      mbar_init(a_empty0 + 8 * i, 1);
+      mbar_init(epi0 + 8 * i, kBlockTiles);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kBlockTiles);
+    mbar_init(mma_done, 1);
+    mbar_init_fence();
+  }
+  if (warp == kTcMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sbase + P::kOffMisc),
+                 "n"(P::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  bool bail = false;
+
+  if (warp == kTcProducer) {
+    // ---------------------------------------------------------------- weight records
+    const uint64_t pol_w = policy_evict_first();
+    // tile_ptr[wb .. wb+95] held across the lanes in three registers; the third
+    // is loaded 8 units before any shuffle reads it.
+    int64_t wb = 4 * u0;
+    const int64_t TT = 4 * a.T;
+    uint32_t w0 = wb + lane <= TT ? __ldg(a.tile_ptr + wb + lane) : 0u;
+    uint32_t w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
+    uint32_t w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
+    int issued = 0, s = 0;
+    uint32_t ph = 0;  // parity of the empty phase to wait for, once the ring has wrapped
+    for (int j = 0; j < nun; ++j) {
+      const int64_t u = u0 + j;
+      if (j >= S) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(rec_empty0 + 8 * s, ph);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          bail = true;
+          break;
+        }
+      }
+      if (4 * u - wb >= 32) {
+        w0 = w1;
+        w1 = w2;
+        wb += 32;
+        w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
+      }
+      const int d = (int)(4 * u - wb);
+      const int src = d + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4u + i]
+      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
+      const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
+      const uint32_t tpv = src < 32 ? v0 : v1;
+      const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
+      const uint32_t e0 = t_first & ~3u;
+      uint32_t e1 = (t_last + 3u) & ~3u;
+      if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
+      const uint32_t esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
+      uint8_t* rec = smem + P::kOffRec + s * P::kRec;
+      if (lane < 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = tpv;
+      if (lane == 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[5] = e0;
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t full = rec_full0 + 8 * s;
+        const uint32_t recs = sbase + P::kOffRec + s * P::kRec;
+        mbar_arrive_expect_tx(full, P::kHi + P::kLo + esc_bytes);
+        bulk_g2s(recs, a.hi + u * P::kHi, P::kHi, full, pol_w);
+        if (!Q8) bulk_g2s(recs + P::kOffLo, a.lo + u * (kBlockTiles * kLoTileBytes), P::kLo, full, pol_w);
+        if (esc_bytes) bulk_g2s(recs + P::kOffEsc, a.esc + e0, esc_bytes, full, pol_w);
+      }
+      issued = j + 1;
+      if (++s == S) {
+        s = 0;
+        if (j >= S) ph ^= 1u;
+      }
+    }
+    // copies still in flight land before the CTA leaves (they have, unless a wait gave up)
+    if (lane == 0)
+      for (int j = std::max(0, issued - S); j < issued; ++j)
+        mbar_wait_bounded(rec_full0 + 8 * (j % S), (uint32_t)((j / S) & 1));
+    __syncwarp();
+  } else if (warp == kTcX) {
+    // ---------------------------------------------------------------- x chunks
+    if (lane == 0) {
+      // x may be the previous kernel's output: wait for that grid to complete and its
+      // writes to be visible.  Every store of this kernel (y, slots, counters) follows an
+      // MMA that reads x, so it also comes after the previous grid has finished.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      const uint64_t pol_x = policy_evict_last();
+      int64_t kc = u0 % a.KC;
+      int issued = 0;
+      for (int j = 0; j < nun; ++j) {
+        const int s = j % SX;
+        if (j >= SX && !mbar_wait_bounded(x_empty0 + 8 * s, (uint32_t)(((j / SX) - 1) & 1))) {
+          bail = true;
+          break;
+        }
+        const uint32_t xfull = x_full0 + 8 * s;
+        mbar_arrive_expect_tx(xfull, P::kX);
+        tma_x(sbase + s * P::kX, &xmap, (int)(kc * kTileK), a.tok0, xfull, pol_x);
+        issued = j + 1;
+        if (++kc == a.KC) kc = 0;
+      }
+      for (int j = std::max(0, issued - SX); j < issued; ++j)
+        mbar_wait_bounded(x_full0 + 8 * (j % SX), (uint32_t)((j / SX) & 1));
+    }
+    __syncwarp();
+  } else if (warp == kTcMma) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc<NT>();
+      int64_t kc = u0 % a.KC;
+      int seg = 0;
+      for (int j = 0; j < nun; ++j) {
+        const int s = j % SX, gi = j & 1;
+        const bool first = (j == 0) || (kc == 0);
+        if (first && j > 0 && !mbar_wait_bounded(acc_empty, (uint32_t)((seg - 1) & 1))) {
+          bail = true;
+          break;
+        }
+        if (!mbar_wait_bounded(a_full0 + 8 * gi, (uint32_t)((j >> 1) & 1)) ||
+            !mbar_wait_bounded(x_full0 + 8 * s, (uint32_t)((j / SX) & 1))) {
+          bail = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t abase = sbase + P::kOffA + gi * kABuf, xbase = sbase + s * P::kX;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem, umma_desc(abase + ks * 32), umma_desc(xbase + ks * 32), idesc, (first && ks == 0) ? 0u : 1u);
+        umma_commit(a_empty0 + 8 * gi);
+        umma_commit(x_empty0 + 8 * s);
+        if ((kc + 1 == a.KC) || (j + 1 == nun)) {
+          umma_commit(acc_full);
+          ++seg;
+        }
+        if (++kc == a.KC) kc = 0;
+      }
+      // every MMA issued here has finished before TMEM is released
+      umma_commit(mma_done);
+      mbar_wait_bounded(mma_done, 0u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- decode warps
+    // Group gi visits only its own units j = gi, gi+2, ...; row block, chunk,
+    // ring stage and phase advance by two units per step.  Unit indices fit in
+    // 32 bits (the host caps T).
+    const int gi = warp >> 2, tl = warp & 3;  // group, row tile inside the block
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t* atp = smem + P::kOffA + gi * kABuf + tl * (kTileRows * 128);
+    const uint32_t a_full = a_full0 + 8 * gi, a_empty = a_empty0 + 8 * gi, epi_bar = epi0 + 8 * gi;
+    const int KC = (int)a.KC, U0 = (int)u0;
+    const int rb0 = U0 / KC;
+    int j = gi;
+    int rb = (U0 + j) / KC, kc = (U0 + j) - rb * KC;
+    int s = j % S;
+    uint32_t ph = (uint32_t)((j / S) & 1);
+    int cur_rb = -1, mine = 0;
+    uint32_t base2[4];
+    uint32_t epi_phase = 0;
+    for (; j < nun; j += 2) {
+      if (rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
+        cur_rb = rb;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t n = ((int64_t)rb * kBlockTiles + tl) * kTileRows + 8 * q + g;
+          const uint32_t bb = n < a.N ? (uint32_t)__ldg(a.base + n) : 1u;
+          base2[q] = (bb << 7) | (bb << 23);
+        }
+      }
+      if (!warp_wait(rec_full0 + 8 * s, ph)) {
+        bail = true;
+        break;
+      }
+      {
+        const uint8_t* rec = smem + P::kOffRec + s * P::kRec;
+        uint4 hq[4];
+        uint2 lq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hq[q] = *reinterpret_cast<const uint4*>(rec + tl * kHiTileBytes + q * 512 + lane * 16);
+          lq[q] = Q8 ? make_uint2(0u, 0u)
+                     : *reinterpret_cast<const uint2*>(rec + P::kOffLo + tl * kLoTileBytes + q * 256 + lane * 8);
+        }
+        // this row tile's escapes: entry ta + lane into a register (the rare tail past 32 stays in memory)
+        const uint32_t* hdr = reinterpret_cast<const uint32_t*>(rec + P::kOffHdr);
+        const uint32_t ta = hdr[tl], tb = hdr[tl + 1], e0 = hdr[5];
+        const uint32_t cnt = tb - ta;
+        uint32_t ent = 0u;
+        if ((uint32_t)lane < cnt) {
+          const uint32_t e = ta + lane;
+          ent = e - e0 < (uint32_t)kEscRun ? reinterpret_cast<const uint32_t*>(rec + P::kOffEsc)[e - e0]
+                                           : __ldg(a.esc + e);
+        }
+        // the record stage can be refilled now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rec_empty0 + 8 * s);
+        // the group's A buffer is free once the MMA of its previous unit has finished
+        // (issued while the other group decoded, so this wait rarely blocks)
+        if (mine > 0 && !warp_wait(a_empty, (uint32_t)((mine - 1) & 1))) {
+          bail = true;
+          break;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pr[8];
+          decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr);
+          uint8_t* row = atp + (8 * q + g) * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+        }
+        __syncwarp();
+        if ((uint32_t)lane < cnt) {
+          const int er = esc_row(ent), ek = esc_col(ent);
+          *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
+              (uint16_t)esc_raw(ent);
+        }
+        if (cnt > 32u) {
+          for (uint32_t e = ta + 32 + lane; e < tb; e += 32) {
+            const uint32_t en = __ldg(a.esc + e);
+            const int er = esc_row(en), ek = esc_col(en);
+            *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
+                (uint16_t)esc_raw(en);
+          }
+        }
+        fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full);
+        ++mine;
+      }
+      if (kc == KC - 1 || j == nun - 1) {
+        // ---- this unit ends a row block (or the CTA's share of one): the accumulator
+        // from TMEM.  seg counts the segments of this CTA before this one.  The previous
+        // segment's drain (possibly by the other group) ends first; after it the
+        // accumulator barrier is at most one phase from this segment's, so its parity
+        // wait is exact.
+        const int seg = rb - rb0;
+        if (seg > 0 && !warp_wait(acc_empty, (uint32_t)((seg - 1) & 1))) {
+          bail = true;
+          break;
+        }
+        if (!warp_wait(acc_full, (uint32_t)(seg & 1))) {
+          bail = true;
+          break;
+        }
+        tc_fence_after();
+        const int64_t rt = (int64_t)rb * kBlockTiles + tl;
+        const bool whole = U0 <= rb * KC && kc == KC - 1;
+        const uint32_t trow = tmem + ((uint32_t)(tl * 32) << 16);
+        if (whole) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(trow + c0, v);
+            emit_cols<EPI>(a, rt, lane, c0, v);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        } else {
+          const int64_t cf = cta_of_unit((int64_t)rb * KC, a.G, a.T);
+          const int64_t cl = cta_of_unit((int64_t)(rb + 1) * KC - 1, a.G, a.T);
+          const int64_t ncov = cl - cf + 1;
+          constexpr int kWarpSlot = NT * 32;  // floats per warp in a slot
+          float4* slot = reinterpret_cast<float4*>(a.slots + ((b + rb) * kBlockTiles + tl) * kWarpSlot);
+#pragma unroll 1
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(trow + c0, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              __stcg(slot + (c0 / 4 + i) * 32 + lane, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+          __threadfence();
+          if (!epi_sync(epi_bar, epi_phase, lane)) {
+            bail = true;
+            break;
+          }
+          if (tl == 0 && lane == 0) misc[1 + gi] = atomicAdd(a.counters + rb, 1u);
+          if (!epi_sync(epi_bar, epi_phase, lane)) {
+            bail = true;
+            break;
+          }
+          const bool emit = (int64_t)misc[1 + gi] == ncov - 1;
+          if (!epi_sync(epi_bar, epi_phase, lane)) {
+            bail = true;
+            break;
+          }
+          if (emit) {
+            __threadfence();
+            if (tl == 0 && lane == 0) a.counters[rb] = 0u;
+#pragma unroll 1
+            for (int c0 = 0; c0 < NT; c0 += 16) {
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              for (int64_t jj = 0; jj < ncov; ++jj) {
+                const float4* sj =
+                    reinterpret_cast<const float4*>(a.slots + ((cf + rb + jj) * kBlockTiles + tl) * kWarpSlot);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float4 q4 = __ldcg(sj + (c0 / 4 + i) * 32 + lane);
+                  v[4 * i] += q4.x;
+                  v[4 * i + 1] += q4.y;
+                  v[4 * i + 2] += q4.z;
+                  v[4 * i + 3] += q4.w;
+                }
+              }
+              emit_cols<EPI>(a, rt, lane, c0, v);
+            }
+          }
+        }
+      }
+      // two units on
+      s += 2;
+      if (s >= S) {
+        s -= S;
+        ph ^= 1u;
+      }
+      kc += 2;
+      while (kc >= KC) {
+        kc -= KC;
+        ++rb;
+      }
+    }
+  }
+
+  // ---- teardown: every warp reaches this point, TMEM is always freed
+  if (bail && lane == 0) atomicOr(a.error, 1u);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcMma)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(P::kTmemCols) : "memory");
+}
+
 // Copy of x with row pitch ldx (a multiple of 8 elements), zero past K.
 __global__ void k_pad_x(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint16_t* __restrict__ xp) {
   const int64_t total = M * ldx;
@@ -441,9 +952,29 @@ int device_sms(int* sms) {
   return W12_OK;
 }
 
+#ifndef W12_GEMM_TC
+#define W12_GEMM_TC 1
+#endif
+#ifndef W12_PDL
+#define W12_PDL 1
+#endif
+
+// Launch shape for M tokens: tokens per launch (the MMA's N) and CTAs per SM.
+struct LaunchShape {
+  int nt, bpsm;
+};
+LaunchShape launch_shape(int64_t M) {
+  if (W12_GEMM_TC) {
+    const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    return {nt, nt <= 32 ? W12_TC_SMALL_BPSM : 1};
+  }
+  const int64_t Mg = std::min<int64_t>(M, kMaxTokens);
+  return {Mg <= 8 ? 8 : Mg <= 16 ? 16 : 32, kBlocksPerSM};
+}
+
 // CTAs of the stream-K partition for a T-unit problem.
-int64_t partition_ctas(int64_t T, int sms) {
-  const int64_t resident = (int64_t)sms * kBlocksPerSM;
+int64_t partition_ctas(int64_t T, int sms, int bpsm) {
+  const int64_t resident = (int64_t)sms * bpsm;
   const int64_t g = (T + kMinIters - 1) / kMinIters;
   return std::max<int64_t>(1, std::min(g, resident));
 }
@@ -456,16 +987,15 @@ struct WsLayout {
 
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   const int64_t RB = row_blocks(N), RT = row_tiles(N), KC = k_chunks(K), T = RB * KC;
-  const int64_t G = partition_ctas(T, sms);
-  const int64_t Mg = std::min<int64_t>(M, kMaxTokens);
-  const int64_t nb = Mg <= 8 ? 1 : Mg <= 16 ? 2 : 4;
+  const LaunchShape ls = launch_shape(M);
+  const int64_t G = partition_ctas(T, sms, ls.bpsm);
   WsLayout L{};
   L.counters = 0;
   size_t off = align256((size_t)RB * 4);
   L.error = off;
   off += 256;
-  L.slots = off;
-  off = align256(off + (size_t)(RB + G) * kConsumers * (size_t)(2 * nb * 4 * 32) * 4);
+  L.slots = off;  // one slot of 128 channels x nt tokens per (CTA, row block) pair
+  off = align256(off + (size_t)(RB + G) * (size_t)(kBlockTiles * kTileRows) * (size_t)ls.nt * 4);
   L.xpad = off;
   off = align256(off + (size_t)M * (size_t)(KC * kTileK) * 2);
   L.pbest = off;
@@ -517,6 +1047,42 @@ int launch_one(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   return W12_OK;
 }
 
+template <int NT, bool Q8, int EPI>
+int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  constexpr int smem = TcPlan<NT, Q8>::kBytes;
+  static int configured_for_device[64] = {0};
+  int dev = 0;
+  W12_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= 64 || !configured_for_device[dev]) {
+    W12_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc<NT, Q8, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    if (dev < 64) configured_for_device[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.G);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = W12_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gemm_tc<NT, Q8, EPI>, map, a));
+  W12_LAUNCH_CHECK("w12 gemm kernel (tcgen05)");
+  return W12_OK;
+}
+
+template <bool Q8, int EPI>
+int launch_nt(int nt, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  switch (nt) {
+    case 16: return launch_tc<16, Q8, EPI>(map, a, s);
+    case 32: return launch_tc<32, Q8, EPI>(map, a, s);
+    case 64: return launch_tc<64, Q8, EPI>(map, a, s);
+    case 128: return launch_tc<128, Q8, EPI>(map, a, s);
+    default: return launch_tc<256, Q8, EPI>(map, a, s);
+  }
+}
+
 template <bool Q8, int EPI>
 int launch_nb(int nb, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   switch (nb) {
@@ -541,6 +1107,9 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   if (ws_bytes < L.total)
     return fail(W12_ERR_BUFFER_TOO_SMALL, "%s: workspace %zu bytes < %zu required", fn, ws_bytes, L.total);
   const int64_t RB = row_blocks(A->N), RT = row_tiles(A->N), KC = k_chunks(A->K), T = RB * KC;
+  if (T >= (int64_t(1) << 30))
+    return fail(W12_ERR_SHAPE, "%s: %lld row blocks x %lld column chunks exceed 2^30 units", fn, (long long)RB,
+                (long long)KC);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
   // x through a tensor map needs a 16-byte aligned base and a row pitch that is a multiple of 16 bytes
@@ -565,27 +1134,36 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.N = A->N;
   a.KC = KC;
   a.T = T;
-  a.G = partition_ctas(T, sms);
+  const LaunchShape ls = launch_shape(M);
+  a.G = partition_ctas(T, sms, ls.bpsm);
   a.ldy = A->N;
   a.slots = reinterpret_cast<float*>(wsb + L.slots);
   a.counters = reinterpret_cast<uint32_t*>(wsb + L.counters);
   a.error = reinterpret_cast<uint32_t*>(wsb + L.error);
   a.pbest = reinterpret_cast<unsigned long long*>(wsb + L.pbest);
   a.ldp = M;
-  a.mul = DecodeMul{16u, 256u, 1u << 28};
-  const int64_t Mg0 = std::min<int64_t>(M, kMaxTokens);
-  const int nb = Mg0 <= 8 ? 1 : Mg0 <= 16 ? 2 : 4;
+  a.mul = W12_DECODE_MUL;
   CUtensorMap map;
-  if ((st = make_x_map(&map, xs, M, A->K, ldx, 8 * nb))) return st;
-  for (int64_t m0 = 0; m0 < M; m0 += kMaxTokens) {
-    const int Mg = (int)std::min<int64_t>(kMaxTokens, M - m0);
+  if ((st = make_x_map(&map, xs, M, A->K, ldx, ls.nt))) return st;
+  for (int64_t m0 = 0; m0 < M; m0 += ls.nt) {
+    const int Mg = (int)std::min<int64_t>(ls.nt, M - m0);
     a.M = Mg;
     a.tok0 = (int)m0;
-    if (!argmax) {
-      a.y = y + m0 * A->N;
-      st = q8 ? launch_nb<true, EPI_STORE>(nb, map, a, s) : launch_nb<false, EPI_STORE>(nb, map, a, s);
+    if (W12_GEMM_TC) {
+      if (!argmax) {
+        a.y = y + m0 * A->N;
+        st = q8 ? launch_nt<true, EPI_STORE>(ls.nt, map, a, s) : launch_nt<false, EPI_STORE>(ls.nt, map, a, s);
+      } else {
+        st = q8 ? launch_nt<true, EPI_ARGMAX>(ls.nt, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls.nt, map, a, s);
+      }
     } else {
-      st = q8 ? launch_nb<true, EPI_ARGMAX>(nb, map, a, s) : launch_nb<false, EPI_ARGMAX>(nb, map, a, s);
+      const int nb = ls.nt / 8;
+      if (!argmax) {
+        a.y = y + m0 * A->N;
+        st = q8 ? launch_nb<true, EPI_STORE>(nb, map, a, s) : launch_nb<false, EPI_STORE>(nb, map, a, s);
+      } else {
+        st = q8 ? launch_nb<true, EPI_ARGMAX>(nb, map, a, s) : launch_nb<false, EPI_ARGMAX>(nb, map, a, s);
+      }
     }
     if (st) return st;
   }

@@ -87,20 +87,36 @@ int check_matrix(const w12_matrix* A, bool need_lo, const char* fn);
 // Word H_s of the hi slice holds the front bytes of columns 4s, 4s+2, 4s+1,
 // 4s+3 (bytes 0..3), so bytes 0,2 give pair 2s and bytes 1,3 give pair 2s+1.
 // A lane's bf16 is s<<15 | (base + eo)<<7 | m6..4<<4 | m3..0 from a front byte
-// f = s<<7 | eo<<3 | m6..4 and a nibble.  The byte spreading runs on the
-// multiply-add pipe (integer multiplies by 16, 256 and 2^28 as shifts), which
-// leaves the logic pipe with two masks and one merge per pair.
+// f = s<<7 | eo<<3 | m6..4 and a nibble.  The nibbles of pair p sit in lo word
+// p/4 at bits 4(p%4) and 16+4(p%4).
+//
+// The work is split between the two integer pipes: masks and merges on the
+// logic pipe, every shift on the multiply-add pipe (x*16 and x*256 move bytes
+// left; the high word of x*2^(32-k) is x>>k, and mad.hi adds it to the partly
+// built pair in the same instruction, which is exact because the target bits
+// are still zero).  Per 16 weights that is 24 logic and 18 multiply-add
+// instructions.
 __device__ __forceinline__ uint32_t mul_hi_add(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
-// The multipliers come in as run-time values (16, 256, 2^28) so that the
-// compiler keeps them as integer multiply-adds instead of logic-pipe shifts.
+// The multipliers come in as run-time values (16, 256 and 2^(32-k) for k = 4,
+// 8, 12) so that the compiler keeps them as integer multiply-adds instead of
+// logic-pipe shifts.
 struct DecodeMul {
-  uint32_t m16, m256, m2p28;
+  uint32_t m16, m256, m2p28, m2p24, m2p20;
 };
+#define W12_DECODE_MUL DecodeMul{16u, 256u, 1u << 28, 1u << 24, 1u << 20}
+
+// nibbles k*4 and 16+k*4 of L added at bits 0 and 16 of v (k = 0..3)
+template <int K>
+__device__ __forceinline__ uint32_t add_nibbles(uint32_t v, uint32_t L, const DecodeMul& m) {
+  if (K == 0) return (L & 0x000F000Fu) | v;
+  const uint32_t mul = K == 1 ? m.m2p28 : K == 2 ? m.m2p24 : m.m2p20;
+  return mul_hi_add(L & (0x000F000Fu << (4 * K)), mul, v);
+}
 
 template <bool Q8>
 __device__ __forceinline__ void decode16(uint4 h, uint2 l, uint32_t base2, const DecodeMul& k, uint32_t out[8]) {
@@ -109,17 +125,22 @@ __device__ __forceinline__ void decode16(uint4 h, uint2 l, uint32_t base2, const
   for (int s = 0; s < 4; ++s) {
     const uint32_t Hs = H[s];
     const uint32_t L = (s < 2) ? l.x : l.y;
-    // pair 2s: bytes 0 and 2 -> (f & 0x7F) * 16 + base<<7, then sign * 256
+    // pair 2s: bytes 0 and 2 -> (f & 0x7F) * 16 + base<<7, sign * 256
     const uint32_t e7 = Hs & 0x007F007Fu;
     const uint32_t es = Hs & 0x00800080u;
     uint32_t ve = es * k.m256 + (e7 * k.m16 + base2);
-    // pair 2s+1: bytes 1 and 3 -> ((f & 0x7F) << 8) >> 4 via the high product, sign already at bit 15
+    // pair 2s+1: bytes 1 and 3 -> (f & 0x7F00) >> 4 via the high product, sign already at bit 15
     const uint32_t o7 = Hs & 0x7F007F00u;
     uint32_t vo = mul_hi_add(o7, k.m2p28, base2) | (Hs & 0x80008000u);
     if (!Q8) {
-      const int p = 2 * s;  // nibble positions 4*(p&3) and 4*((p+1)&3)
-      ve |= (L >> (4 * (p & 3))) & 0x000F000Fu;
-      vo |= (L >> (4 * ((p + 1) & 3))) & 0x000F000Fu;
+      // pair 2s has p%4 = 2s%4 in {0, 2}; pair 2s+1 has p%4 in {1, 3}
+      if ((s & 1) == 0) {
+        ve = add_nibbles<0>(ve, L, k);
+        vo = add_nibbles<1>(vo, L, k);
+      } else {
+        ve = add_nibbles<2>(ve, L, k);
+        vo = add_nibbles<3>(vo, L, k);
+      }
     }
     out[2 * s] = ve;
     out[2 * s + 1] = vo;
@@ -209,29 +230,26 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 #ifndef W12_NAP_NS
-#define W12_NAP_NS 32
+#define W12_NAP_NS -1
 #endif
-// Waits for the barrier phase with a clock limit (about 2^31 cycles, ~1 s);
-// returns false when the limit ran out.  It polls with test_wait (which never
-// blocks) and naps a few tens of ns between polls: a thread suspended inside
-// try_wait was measured to notice a completed phase up to ~0.8 us late, while
-// a napping warp still leaves its scheduler's issue slots to the others.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (W12_NAP_NS < 0) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long start = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-      if (clock64() - start > (1ll << 31)) return false;
-    }
-    return true;
-  }
-  if (mbar_test_wait(bar, parity)) return true;
+// Slow path of mbar_wait_bounded: try_wait (the thread may be suspended in
+// hardware until the phase completes), or with W12_NAP_NS >= 0 test_wait polls
+// with that many ns of sleep between them, up to a clock limit of about 2^31
+// cycles (~1 s).  Returns false when the limit ran out.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const long long start = clock64();
-  while (!mbar_test_wait(bar, parity)) {
+  while (!(W12_NAP_NS < 0 ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity))) {
     if (W12_NAP_NS > 0) __nanosleep(W12_NAP_NS);
     if (clock64() - start > (1ll << 31)) return false;
   }
   return true;
+}
+
+// Waits for the barrier phase with parity `parity`, bounded; one non-blocking
+// test first, so a phase that has already completed costs two instructions.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 
 // Global -> shared bulk copy completing on an mbarrier (size multiple of 16, both addresses 16-byte aligned).
