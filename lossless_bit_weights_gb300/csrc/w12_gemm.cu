@@ -1,27 +1,32 @@
-// w12_gemm.cu - decode-fused weight-streaming GEMM for few rows (up to 32
+// w12_gemm.cu - decode-fused weight-streaming GEMM for few rows (up to 256
 // tokens per launch), its 8-bit-view variant, and the LM-head argmax epilogue.
 //
 // The SpecPilot summary page (onedev.kr/papers/1654), section "What's
 // different", describes a GEMM that decodes the 12-bit records in registers,
 // hides the decode behind the memory stream and stays deterministic with
 // stream-K.  This kernel is built for sm_103a:
-//  - one CTA = 1 producer warp + 4 consumer warps; a unit of work is a row
-//    block (128 channels = 4 row tiles) x one 64-column chunk;
-//  - the producer fills a 3-stage shared-memory ring with bulk copies (TMA):
-//    the block's 8 KB of front bytes and 4 KB of nibbles (adjacent in the
-//    device tile order), the block's escape run, and the chunk of x through a
-//    2-D tensor map (128-byte swizzle; rows past M and columns past K read as
-//    zero);
-//  - each consumer warp decodes its 32x64 tile in registers to bf16 (sign,
-//    base+offset, mantissa), stores it to a swizzled tile, writes the tile's
-//    escapes over their slots, and runs mma.sync m16n8k16 with the weights as
-//    the 16-row A operand and the tokens as 8-column B blocks (swap-AB), both
-//    through ldmatrix;
-//  - the flat list of (row block, chunk) units is split evenly over CTAs
-//    (stream-K).  A CTA that owns part of a row block writes partial sums to
-//    a fixed slot; the last CTA of that block to arrive (atomic counter, no
-//    waiting) adds the slots in slot order, so results are bit-identical
-//    from call to call.
+//  - a unit of work is a row block (128 channels = 4 row tiles) x one
+//    64-column chunk; the flat list of units is split evenly over the CTAs
+//    (stream-K);
+//  - one producer warp fills a shared-memory ring with bulk copies (TMA): the
+//    block's 8 KB of front bytes and 4 KB of nibbles (adjacent in the device
+//    tile order) and its escape run; another warp streams the chunk of x
+//    through a 2-D tensor map (128-byte swizzle; rows past M and columns past
+//    K read as zero);
+//  - two groups of four decode warps take alternate units; each warp decodes
+//    its 32x64 tile in registers to bf16 (sign, base+offset, mantissa), stores
+//    it to the group's swizzled A buffer and writes the tile's escapes over
+//    their slots;
+//  - one thread issues tcgen05.mma (M = 128 channels, N = 16..256 tokens,
+//    swap-AB: weights on the M side) with the fp32 accumulator in tensor
+//    memory; at the end of a row block the group that decoded its last unit
+//    reads the accumulator back;
+//  - a CTA that owns part of a row block writes partial sums to a fixed slot;
+//    the last CTA of that block to arrive (atomic counter, no waiting) adds
+//    the slots in slot order, so results are bit-identical from call to call;
+//  - launches use programmatic dependent launch: a GEMM starts streaming its
+//    weights while the previous kernel on the stream drains, and waits for
+//    that kernel only before it reads x.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -34,28 +39,8 @@
 namespace w12 {
 namespace {
 
-constexpr int kConsumers = kBlockTiles;          // consumer warps, one row tile each
-constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
-constexpr int kATile = kTileRows * 128;          // decoded 32x64 bf16 tile (swizzled)
-constexpr int kEscRun = 128;                     // escape entries a stage holds
-#ifndef W12_GEMM_STAGES
-#define W12_GEMM_STAGES 3
-#endif
-#ifndef W12_GEMM_PREFETCH
-#define W12_GEMM_PREFETCH 0
-#endif
-#ifndef W12_GEMM_BLOCKS_PER_SM
-#define W12_GEMM_BLOCKS_PER_SM 3
-#endif
-constexpr int kBlocksPerSM = W12_GEMM_BLOCKS_PER_SM;
-#ifdef W12_CONST_MUL
-#define W12_KMUL W12_DECODE_MUL
-#else
-#define W12_KMUL a.mul
-#endif
-constexpr int kMinIters = 4;                     // fewest units per CTA
-constexpr int kMaxTokens = 32;                   // tokens per launch
-constexpr int kPrefetch = W12_GEMM_PREFETCH;      // units warmed in L2 ahead of the ring
+constexpr int kEscRun = 128;  // escape entries a record stage holds
+constexpr int kMinIters = 4;  // fewest units per CTA
 
 enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1 };
 
@@ -66,7 +51,7 @@ struct GemmArgs {
   const uint32_t* tile_ptr;
   const uint32_t* esc;
   int64_t N, KC, T, G;  // T = row blocks * KC units, G = CTAs of the partition
-  int M;                // tokens of this launch (<= 8*NB)
+  int M;                // tokens of this launch (<= NT)
   int tok0;             // first token of this launch (x tensor-map row)
   float* y;             // EPI_STORE: y[m*ldy + n] (already offset to tok0)
   int64_t ldy;
@@ -76,23 +61,6 @@ struct GemmArgs {
   uint32_t* counters;
   uint32_t* error;
   DecodeMul mul;
-};
-
-// Shared-memory plan: [x stages (1 KB aligned)][record stages][A tiles][barriers]
-template <int NB, bool Q8>
-struct Plan {
-  static constexpr int kStages = W12_GEMM_STAGES;
-  static constexpr int kX = 8 * NB * 128;                     // swizzled x chunk
-  static constexpr int kHi = kBlockTiles * kHiTileBytes;      // 8 KB
-  static constexpr int kLo = Q8 ? 0 : kBlockTiles * kLoTileBytes;
-  static constexpr int kOffLo = kHi;
-  static constexpr int kOffEsc = kHi + kLo;
-  static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
-  static constexpr int kRec = kOffHdr + 32;
-  static constexpr int kOffRec = kStages * kX;
-  static constexpr int kOffA = kOffRec + kStages * kRec;
-  static constexpr int kOffBar = kOffA + kConsumers * kATile;
-  static constexpr int kBytes = kOffBar + kStages * 16 + 16;
 };
 
 __device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
@@ -109,313 +77,30 @@ __device__ __forceinline__ void tma_x(uint32_t dst, const CUtensorMap* map, int 
       : "memory");
 }
 
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
-
-template <int NB, bool Q8, int EPI>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemm(const __grid_constant__ CUtensorMap xmap,
-                                                                  const GemmArgs a) {
-  using P = Plan<NB, Q8>;
-  constexpr int S = P::kStages;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint32_t last_flag;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t b = blockIdx.x;
-  if (b >= a.G) return;
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t full0 = sbase + P::kOffBar, empty0 = full0 + 8 * S;
-  const int64_t u0 = b * a.T / a.G, u1 = (b + 1) * a.T / a.G;
-  const int nun = (int)(u1 - u0);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kConsumers);
-    }
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  if (warp == kConsumers) {
-    // ================================================================ producer
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    // tile_ptr[wb .. wb+95] held across the lanes in three registers; the third
-    // is loaded 8 units before any shuffle reads it, so the loop never waits on it.
-    int64_t wb = 4 * u0;
-    const int64_t TT = 4 * a.T;
-    uint32_t w0 = wb + lane <= TT ? __ldg(a.tile_ptr + wb + lane) : 0u;
-    uint32_t w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
-    uint32_t w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
-    int64_t kc = u0 % a.KC;
-    if (kPrefetch > 0 && lane == 0)
-      for (int j = S; j < S + kPrefetch && j < nun; ++j) {
-        prefetch_l2(a.hi + (u0 + j) * P::kHi, P::kHi);
-        if (!Q8) prefetch_l2(a.lo + (u0 + j) * (kBlockTiles * kLoTileBytes), P::kLo);
-      }
-    for (int j = 0; j < nun; ++j) {
-      const int s = j % S;
-      const int64_t u = u0 + j;
-      if (kPrefetch > 0 && lane == 0 && j + S + kPrefetch < nun) {
-        const int64_t up = u + S + kPrefetch;
-        prefetch_l2(a.hi + up * P::kHi, P::kHi);
-        if (!Q8) prefetch_l2(a.lo + up * (kBlockTiles * kLoTileBytes), P::kLo);
-      }
-      if (j >= S && !mbar_wait_bounded(empty0 + 8 * s, (uint32_t)(((j / S) - 1) & 1))) {
-        if (lane == 0) atomicOr(a.error, 1u);
-        return;
-      }
-      if (4 * u - wb >= 32) {
-        w0 = w1;
-        w1 = w2;
-        wb += 32;
-        w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
-      }
-      const int d = (int)(4 * u - wb);
-      // lane i < 5 gets tile_ptr[4u + i]
-      const int src = d + (lane < 5 ? lane : 0);
-      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
-      const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
-      const uint32_t tpv = src < 32 ? v0 : v1;
-      const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
-      const uint32_t e0 = t_first & ~3u;
-      uint32_t e1 = (t_last + 3u) & ~3u;
-      if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
-      const uint32_t esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
-      uint8_t* rec = smem + P::kOffRec + s * P::kRec;
-      if (lane < 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = tpv;
-      if (lane == 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[5] = e0;
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t full = full0 + 8 * s;
-        const uint32_t recs = sbase + P::kOffRec + s * P::kRec;
-        mbar_arrive_expect_tx(full, P::kHi + P::kLo + P::kX + esc_bytes);
-        bulk_g2s(recs, a.hi + u * P::kHi, P::kHi, full, pol_w);
-        if (!Q8) bulk_g2s(recs + P::kOffLo, a.lo + u * (kBlockTiles * kLoTileBytes), P::kLo, full, pol_w);
-        if (esc_bytes) bulk_g2s(recs + P::kOffEsc, a.esc + e0, esc_bytes, full, pol_w);
-        tma_x(sbase + s * P::kX, &xmap, (int)(kc * kTileK), a.tok0, full, pol_x);
-      }
-      if (++kc == a.KC) kc = 0;
-    }
-    return;
-  }
-
-  // ================================================================ consumers
-  const int w = warp;  // row tile inside the block
-  uint8_t* atp = smem + P::kOffA + w * kATile;
-  const uint32_t at = smem_u32(atp);
-  const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
-  float acc[2][NB][4];
-  uint32_t base2[4];
-  int64_t rb = u0 / a.KC;
-  int64_t kc = u0 - rb * a.KC;
-  int64_t seg_start = u0;
-
-  for (int j = 0; j < nun; ++j) {
-    const int64_t u = u0 + j;
-    const int s = j % S;
-    const uint8_t* rec = smem + P::kOffRec + s * P::kRec;
-    if (j == 0 || kc == 0) {  // a new row block starts
-      seg_start = u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t n = (rb * kBlockTiles + w) * kTileRows + 8 * q + g;
-        const uint32_t bb = n < a.N ? (uint32_t)__ldg(a.base + n) : 1u;
-        base2[q] = (bb << 7) | (bb << 23);
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[h][nb][i] = 0.f;
-    }
-    if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)((j / S) & 1))) {
-      if (lane == 0) atomicOr(a.error, 2u);
-      return;
-    }
-    // ---- decode this warp's tile into its swizzled A tile
-    uint4 hq[4];
-    uint2 lq[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      hq[q] = *reinterpret_cast<const uint4*>(rec + w * kHiTileBytes + q * 512 + lane * 16);
-      lq[q] = Q8 ? make_uint2(0u, 0u)
-                 : *reinterpret_cast<const uint2*>(rec + P::kOffLo + w * kLoTileBytes + q * 256 + lane * 8);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t pr[8];
-      decode16<Q8>(hq[q], lq[q], base2[q], W12_KMUL, pr);
-      uint8_t* row = atp + (8 * q + g) * 128;
-      *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-      *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
-    }
-    __syncwarp();
-    // ---- this tile's escapes overwrite their slots with the exact value
-    {
-      const uint32_t* hdr = reinterpret_cast<const uint32_t*>(rec + P::kOffHdr);
-      const uint32_t ta = hdr[w], tb = hdr[w + 1], e0 = hdr[5];
-      const uint32_t* run = reinterpret_cast<const uint32_t*>(rec + P::kOffEsc);
-      for (uint32_t e = ta + lane; e < tb; e += 32) {
-        const uint32_t ent = e - e0 < (uint32_t)kEscRun ? run[e - e0] : __ldg(a.esc + e);
-        const int er = esc_row(ent), ek = esc_col(ent);
-        *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
-            (uint16_t)esc_raw(ent);
-      }
-    }
-    __syncwarp();
-    // ---- tensor-core products: A = weights, B = tokens (ldmatrix on both)
-    const uint32_t xs = sbase + s * P::kX;
-#pragma unroll
-    for (int k16 = 0; k16 < 4; ++k16) {
-      uint32_t bfr[NB][2];
-      if (NB == 1) {
-        ldsm_x2(xs + rr * 128 + (((2 * k16 + (mi & 1)) ^ rr) << 4), bfr[0][0], bfr[0][1]);
-      } else {
-#pragma unroll
-        for (int nb = 0; nb < NB; nb += 2) {
-          const int tok = (nb + (mi >> 1)) * 8 + rr;
-          ldsm_x4(xs + tok * 128 + (((2 * k16 + (mi & 1)) ^ rr) << 4), bfr[nb][0], bfr[nb][1], bfr[nb + 1][0],
-                  bfr[nb + 1][1]);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = 16 * h + (mi & 1) * 8 + rr;
-        const int chunk = 2 * k16 + (mi >> 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(at + row * 128 + ((chunk ^ rr) << 4), a0, a1, a2, a3);
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(acc[h][nb], a0, a1, a2, a3, bfr[nb][0], bfr[nb][1]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive(empty0 + 8 * s);
-    }
-    const bool block_end = (kc + 1 == a.KC);
-    const bool range_end = (j + 1 == nun);
-    if (++kc == a.KC) kc = 0;
-    if (!block_end && !range_end) continue;
-
-    // ---- row block finished (or this CTA's share of it): combine in slot order
-    const bool whole = (seg_start == rb * a.KC) && block_end;
-    bool emit = true;
-    if (!whole) {
-      const int64_t cf = cta_of_unit(rb * a.KC, a.G, a.T);
-      const int64_t cl = cta_of_unit((rb + 1) * a.KC - 1, a.G, a.T);
-      const int64_t ncov = cl - cf + 1;
-      constexpr int kWarpSlot = 2 * NB * 4 * 32;  // floats per warp in a slot
-      float4* slot = reinterpret_cast<float4*>(a.slots + ((cf + rb + (b - cf)) * kConsumers + w) * kWarpSlot);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-          __stcg(slot + (h * NB + nb) * 32 + lane,
-                 make_float4(acc[h][nb][0], acc[h][nb][1], acc[h][nb][2], acc[h][nb][3]));
-      __threadfence();
-      consumers_sync();
-      if (threadIdx.x == 0) last_flag = atomicAdd(a.counters + rb, 1u);
-      consumers_sync();
-      emit = (int64_t)last_flag == ncov - 1;
-      consumers_sync();
-      if (emit) {
-        __threadfence();
-        if (threadIdx.x == 0) a.counters[rb] = 0u;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[h][nb][i] = 0.f;
-        for (int64_t jj = 0; jj < ncov; ++jj) {
-          const float4* sj = reinterpret_cast<const float4*>(a.slots + ((cf + rb + jj) * kConsumers + w) * kWarpSlot);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const float4 v = __ldcg(sj + (h * NB + nb) * 32 + lane);
-              acc[h][nb][0] += v.x;
-              acc[h][nb][1] += v.y;
-              acc[h][nb][2] += v.z;
-              acc[h][nb][3] += v.w;
-            }
-        }
-      }
-    }
-    if (emit) {
-      const int64_t rt = rb * kBlockTiles + w;
-      if (EPI == EPI_STORE) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int64_t n = rt * kTileRows + 16 * h + g + 8 * (i >> 1);
-              const int tok = nb * 8 + 2 * t + (i & 1);
-              if (n < a.N && tok < a.M) a.y[(int64_t)tok * a.ldy + n] = acc[h][nb][i];
-            }
-      } else {
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            unsigned long long best = 0ull;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int64_t n = rt * kTileRows + 16 * h + 8 * hh + g;
-                if (n < a.N) {
-                  const uint32_t key = (uint32_t)order_key(acc[h][nb][2 * hh + e]) ^ 0x80000000u;
-                  const unsigned long long cand =
-                      ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
-                  best = cand > best ? cand : best;
-                }
-              }
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-              const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-              best = other > best ? other : best;
-            }
-            const int tok = nb * 8 + 2 * t + e;
-            if (g == 0 && tok < a.M) a.pbest[rt * a.ldp + a.tok0 + tok] = best;
-          }
-      }
-    }
-    if (block_end) ++rb;
-  }
-}
-
 // ===========================================================================
 // tcgen05 variant: decode warps unpack into shared memory; one thread issues
 // the MMAs (5th-generation tensor core, fp32 accumulator in tensor memory).
-//   warps 0..7   decode, two groups of four: group g takes the units j with
-//                j % 2 == g, warp w of a group the row tile w % 4 (32 rows).
-//                The group that decodes a row block's last unit drains the
-//                accumulator (warp w reads TMEM lanes 32(w%4)..32(w%4)+31).
-//   warp 8       TMA producer of the weight records (hi, lo, escape run)
-//   warp 9       lane 0 issues tcgen05.mma (M=128 channels, N=NT tokens, K=16)
-//   warp 10      lane 0 streams x through the tensor map on its own ring
+//   warps 0..4G-1  decode, G groups of four: group g takes the units j with
+//                  j % G == g, warp w of a group the row tile w % 4 (32 rows).
+//                  The group that decodes a row block's last unit drains the
+//                  accumulator (warp w reads TMEM lanes 32(w%4)..32(w%4)+31).
+//   warp 4G        TMA producer of the weight records (hi, lo, escape run)
+//   warp 4G+1      lane 0 issues tcgen05.mma (M=128 channels, N=NT tokens, K=16)
+//   warp 4G+2      lane 0 streams x through the tensor map on its own ring
 // A record stage goes back to the producer as soon as its group holds the
-// unit in registers; x stages and A buffers go back on the MMA commit.
+// unit in registers; x stages and A buffers go back on the MMA commit.  With
+// four groups a group has four unit-times for its own unit, so a record stage
+// is taken as soon as it lands and the whole shared memory of the SM serves
+// one deep ring.
 constexpr int kTcGroups = 2;
 constexpr int kTcDecoders = kTcGroups * kBlockTiles;
 constexpr int kTcProducer = kTcDecoders, kTcMma = kTcDecoders + 1, kTcX = kTcDecoders + 2;
 constexpr int kTcThreads = (kTcDecoders + 3) * 32;
 constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 block (16 KB, swizzled)
 
-#ifndef W12_TC_SMALL_BPSM
-#define W12_TC_SMALL_BPSM 2
-#endif
-#ifndef W12_TC_MAX_STAGES
-#define W12_TC_MAX_STAGES 16
-#endif
-
 template <int NT, bool Q8>
 struct TcPlan {
-  static constexpr int kBlocksPerSM = NT <= 32 ? W12_TC_SMALL_BPSM : 1;
+  static constexpr int kBlocksPerSM = NT <= 32 ? 2 : 1;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
   static constexpr int kXStages = NT <= 64 ? 4 : 2;
   static constexpr int kHi = kBlockTiles * kHiTileBytes;
@@ -427,15 +112,15 @@ struct TcPlan {
   static constexpr int kOffA = kXStages * kX;                 // one A buffer per decode group
   static constexpr int kOffRec = kOffA + kTcGroups * kABuf;
   static constexpr int kBudget = (kBlocksPerSM == 2 ? 112 : 224) * 1024;
-  static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 16) / kRec;
-  static constexpr int kStages = kStagesRaw > W12_TC_MAX_STAGES ? W12_TC_MAX_STAGES : kStagesRaw;
+  static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
+  static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
-  // rec_full[S] rec_empty[S] x_full[SX] x_empty[SX] a_full[2] a_empty[2] epi[2] acc_full acc_empty mma_done
+  // rec_full[S] rec_empty[S] x_full[SX] x_empty[SX] a_full[G] a_empty[G] epi[G] acc_full acc_empty mma_done
   static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kTcGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
-  static_assert(kStages >= 3, "record ring too shallow");
+  static_assert(kStages >= 3 && kStages > kTcGroups, "record ring too shallow");
   static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
 
@@ -487,6 +172,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
 // Bounded barrier wait whose outcome is the same in every lane of the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity));
+}
+
+// Waits (bounded, warp-uniform) until a shared-memory counter reaches target.
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target) {
+  bool ok = true;
+  if (*reinterpret_cast<const volatile uint32_t*>(c) < target) {
+    const long long start = clock64();
+    while (*reinterpret_cast<const volatile uint32_t*>(c) < target) {
+      __nanosleep(64);
+      if (clock64() - start > (1ll << 31)) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Rendezvous of a decode group's four warps on an mbarrier, bounded.
@@ -541,7 +242,8 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
   const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S, x_full0 = bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
   const uint32_t a_full0 = x_empty0 + 8 * SX, a_empty0 = a_full0 + 8 * kTcGroups, epi0 = a_empty0 + 8 * kTcGroups;
   const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);  // [0] TMEM address, [1+g] stream-K flag
+  // misc: [0] TMEM address, [1+g] stream-K flag of group g, [15] drains finished (four per segment)
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
   const int64_t u0 = b * a.T / a.G, u1 = (b + 1) * a.T / a.G;
   const int nun = (int)(u1 - u0);
 
@@ -549,6 +251,7 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
   // dependent launch): its weight stream does not depend on this kernel's output.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
+    misc[15] = 0u;
     for (int i = 0; i < S; ++i) {
       mbar_init(rec_full0 + 8 * i, 1);
       mbar_init(rec_empty0 + 8 * i, kBlockTiles);
@@ -673,13 +376,13 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
       int64_t kc = u0 % a.KC;
       int seg = 0;
       for (int j = 0; j < nun; ++j) {
-        const int s = j % SX, gi = j & 1;
+        const int s = j % SX, gi = j % kTcGroups;
         const bool first = (j == 0) || (kc == 0);
         if (first && j > 0 && !mbar_wait_bounded(acc_empty, (uint32_t)((seg - 1) & 1))) {
           bail = true;
           break;
         }
-        if (!mbar_wait_bounded(a_full0 + 8 * gi, (uint32_t)((j >> 1) & 1)) ||
+        if (!mbar_wait_bounded(a_full0 + 8 * gi, (uint32_t)((j / kTcGroups) & 1)) ||
             !mbar_wait_bounded(x_full0 + 8 * s, (uint32_t)((j / SX) & 1))) {
           bail = true;
           break;
@@ -704,8 +407,8 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- decode warps
-    // Group gi visits only its own units j = gi, gi+2, ...; row block, chunk,
-    // ring stage and phase advance by two units per step.  Unit indices fit in
+    // Group gi visits only its own units j = gi, gi+G, ...; row block, chunk,
+    // ring stage and phase advance by G units per step.  Unit indices fit in
     // 32 bits (the host caps T).
     const int gi = warp >> 2, tl = warp & 3;  // group, row tile inside the block
     const int g = lane >> 2, t = lane & 3;
@@ -720,7 +423,7 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
     int cur_rb = -1, mine = 0;
     uint32_t base2[4];
     uint32_t epi_phase = 0;
-    for (; j < nun; j += 2) {
+    for (; j < nun; j += kTcGroups) {
       if (rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
         cur_rb = rb;
 #pragma unroll
@@ -757,19 +460,22 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
         // the record stage can be refilled now
         __syncwarp();
         if (lane == 0) mbar_arrive(rec_empty0 + 8 * s);
-        // the group's A buffer is free once the MMA of its previous unit has finished
-        // (issued while the other group decoded, so this wait rarely blocks)
+        // Decode into registers, then wait until the group's A buffer is free (the MMA of
+        // its previous unit has finished), so that the decode overlaps the tensor cores'
+        // work on that unit.
+        uint32_t pr[4][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr[q]);
         if (mine > 0 && !warp_wait(a_empty, (uint32_t)((mine - 1) & 1))) {
           bail = true;
           break;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint32_t pr[8];
-          decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr);
           uint8_t* row = atp + (8 * q + g) * 128;
-          *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-          *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+          *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[q][0], pr[q][1], pr[q][2], pr[q][3]);
+          *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) =
+              make_uint4(pr[q][4], pr[q][5], pr[q][6], pr[q][7]);
         }
         __syncwarp();
         if ((uint32_t)lane < cnt) {
@@ -792,12 +498,11 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
       }
       if (kc == KC - 1 || j == nun - 1) {
         // ---- this unit ends a row block (or the CTA's share of one): the accumulator
-        // from TMEM.  seg counts the segments of this CTA before this one.  The previous
-        // segment's drain (possibly by the other group) ends first; after it the
-        // accumulator barrier is at most one phase from this segment's, so its parity
-        // wait is exact.
+        // from TMEM.  seg counts the segments of this CTA before this one.  The drains of
+        // the earlier segments (by any group) end first; after them the accumulator
+        // barrier is at most one phase from this segment's, so its parity wait is exact.
         const int seg = rb - rb0;
-        if (seg > 0 && !warp_wait(acc_empty, (uint32_t)((seg - 1) & 1))) {
+        if (seg > 0 && !wait_count(misc + 15, 4u * (uint32_t)seg)) {
           bail = true;
           break;
         }
@@ -818,7 +523,10 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
+          if (lane == 0) {
+            mbar_arrive(acc_empty);
+            atomicAdd(misc + 15, 1u);
+          }
         } else {
           const int64_t cf = cta_of_unit((int64_t)rb * KC, a.G, a.T);
           const int64_t cl = cta_of_unit((int64_t)(rb + 1) * KC - 1, a.G, a.T);
@@ -835,7 +543,10 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
+          if (lane == 0) {
+            mbar_arrive(acc_empty);
+            atomicAdd(misc + 15, 1u);
+          }
           __threadfence();
           if (!epi_sync(epi_bar, epi_phase, lane)) {
             bail = true;
@@ -876,13 +587,13 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
           }
         }
       }
-      // two units on
-      s += 2;
+      // G units on (S > G, so the ring wraps at most once)
+      s += kTcGroups;
       if (s >= S) {
         s -= S;
         ph ^= 1u;
       }
-      kc += 2;
+      kc += kTcGroups;
       while (kc >= KC) {
         kc -= KC;
         ++rb;
@@ -952,24 +663,13 @@ int device_sms(int* sms) {
   return W12_OK;
 }
 
-#ifndef W12_GEMM_TC
-#define W12_GEMM_TC 1
-#endif
-#ifndef W12_PDL
-#define W12_PDL 1
-#endif
-
 // Launch shape for M tokens: tokens per launch (the MMA's N) and CTAs per SM.
 struct LaunchShape {
   int nt, bpsm;
 };
 LaunchShape launch_shape(int64_t M) {
-  if (W12_GEMM_TC) {
-    const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-    return {nt, nt <= 32 ? W12_TC_SMALL_BPSM : 1};
-  }
-  const int64_t Mg = std::min<int64_t>(M, kMaxTokens);
-  return {Mg <= 8 ? 8 : Mg <= 16 ? 16 : 32, kBlocksPerSM};
+  const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  return {nt, nt <= 32 ? 2 : 1};
 }
 
 // CTAs of the stream-K partition for a T-unit problem.
@@ -1032,21 +732,6 @@ int make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K, int64_
   return W12_OK;
 }
 
-template <int NB, bool Q8, int EPI>
-int launch_one(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  constexpr int smem = Plan<NB, Q8>::kBytes;
-  static int configured_for_device[64] = {0};
-  int dev = 0;
-  W12_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev >= 64 || !configured_for_device[dev]) {
-    W12_CUDA_TRY(cudaFuncSetAttribute(k_gemm<NB, Q8, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    if (dev < 64) configured_for_device[dev] = 1;
-  }
-  k_gemm<NB, Q8, EPI><<<(unsigned)a.G, kThreads, smem, s>>>(map, a);
-  W12_LAUNCH_CHECK("w12 gemm kernel");
-  return W12_OK;
-}
-
 template <int NT, bool Q8, int EPI>
 int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   constexpr int smem = TcPlan<NT, Q8>::kBytes;
@@ -1064,7 +749,7 @@ int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = W12_PDL;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gemm_tc<NT, Q8, EPI>, map, a));
@@ -1080,15 +765,6 @@ int launch_nt(int nt, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s)
     case 64: return launch_tc<64, Q8, EPI>(map, a, s);
     case 128: return launch_tc<128, Q8, EPI>(map, a, s);
     default: return launch_tc<256, Q8, EPI>(map, a, s);
-  }
-}
-
-template <bool Q8, int EPI>
-int launch_nb(int nb, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  switch (nb) {
-    case 1: return launch_one<1, Q8, EPI>(map, a, s);
-    case 2: return launch_one<2, Q8, EPI>(map, a, s);
-    default: return launch_one<4, Q8, EPI>(map, a, s);
   }
 }
 
@@ -1149,21 +825,11 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
     const int Mg = (int)std::min<int64_t>(ls.nt, M - m0);
     a.M = Mg;
     a.tok0 = (int)m0;
-    if (W12_GEMM_TC) {
-      if (!argmax) {
-        a.y = y + m0 * A->N;
-        st = q8 ? launch_nt<true, EPI_STORE>(ls.nt, map, a, s) : launch_nt<false, EPI_STORE>(ls.nt, map, a, s);
-      } else {
-        st = q8 ? launch_nt<true, EPI_ARGMAX>(ls.nt, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls.nt, map, a, s);
-      }
+    if (!argmax) {
+      a.y = y + m0 * A->N;
+      st = q8 ? launch_nt<true, EPI_STORE>(ls.nt, map, a, s) : launch_nt<false, EPI_STORE>(ls.nt, map, a, s);
     } else {
-      const int nb = ls.nt / 8;
-      if (!argmax) {
-        a.y = y + m0 * A->N;
-        st = q8 ? launch_nb<true, EPI_STORE>(nb, map, a, s) : launch_nb<false, EPI_STORE>(nb, map, a, s);
-      } else {
-        st = q8 ? launch_nb<true, EPI_ARGMAX>(nb, map, a, s) : launch_nb<false, EPI_ARGMAX>(nb, map, a, s);
-      }
+      st = q8 ? launch_nt<true, EPI_ARGMAX>(ls.nt, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls.nt, map, a, s);
     }
     if (st) return st;
   }

@@ -229,17 +229,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-#ifndef W12_NAP_NS
-#define W12_NAP_NS -1
-#endif
 // Slow path of mbar_wait_bounded: try_wait (the thread may be suspended in
-// hardware until the phase completes), or with W12_NAP_NS >= 0 test_wait polls
-// with that many ns of sleep between them, up to a clock limit of about 2^31
+// hardware until the phase completes) up to a clock limit of about 2^31
 // cycles (~1 s).  Returns false when the limit ran out.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const long long start = clock64();
-  while (!(W12_NAP_NS < 0 ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity))) {
-    if (W12_NAP_NS > 0) __nanosleep(W12_NAP_NS);
+  while (!mbar_try_wait(bar, parity)) {
     if (clock64() - start > (1ll << 31)) return false;
   }
   return true;
