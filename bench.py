@@ -54,6 +54,7 @@ def parse_args():
     p.add_argument("--M", type=int, default=16)
     p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack rows (32 GB of W12)")
     p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead"], default=None,
                    help="profiling case: repeat one matrix's GEMM (or the LM head) and print its time")
     p.add_argument("--q8", action="store_true", help="with --only: the 8-bit-view GEMM")
@@ -428,53 +429,169 @@ def run_w12(args, world, rank, local):
 BLOCK_NAMES = [(n, (N, K)) for n, N, K in BLOCK]
 
 
-def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
-    """Q8 pass over the same block and the LM head with fused argmax + tree
-    acceptance, each timed with CUDA events (not part of `value`)."""
-    out = {}
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def timed_ms(torch, fn, n, warm=3):
+    """Average ms of fn over n back-to-back calls, CUDA events around the loop."""
     s = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(n):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def gemm_bytes(A, M, q8=False):
+    return A.stream_bytes(q8=q8) + 2 * M * A.K + 4 * M * A.N
+
+
+def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
+    """The other hot-path rows, each timed with CUDA events (not part of `value`):
+    the Q8 pass over the block at M=16, the LM head with fused argmax + acceptance at
+    M=16, the 64-layer stack at M=32 (exact and Q8 passes, then the W12 head with a
+    32-node tree), and the block and head at M=192 with 24 eight-node trees."""
+    import numpy as np
+    out = {}
     steps = max(5, args.steps // 4)
+    dev = torch.device("cuda", torch.cuda.current_device())
 
-    def timed(fn, n):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        for _ in range(n):
-            fn()
-        b.record(s)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
-
-    ysq = [torch.empty((M, A.N), dtype=torch.float32, device="cuda") for _, A in mats]
+    # ---- Q8 pass over the block at M = 16
+    ysq = [torch.empty((M, A.N), dtype=torch.float32, device=dev) for _, A in mats]
 
     def q8_step():
         for (_, A), x, y in zip(mats, xs, ysq):
             w12.w12_gemm_q8(x, A, y=y, ws=ws)
 
-    ms = timed(q8_step, steps)
+    ms = timed_ms(torch, q8_step, steps)
     weights = sum(A.N * A.K for _, A in mats)
-    qbytes = sum(A.stream_bytes(q8=True) + 2 * M * A.K + 4 * M * A.N for _, A in mats)
+    qbytes = sum(gemm_bytes(A, M, True) for _, A in mats)
     out["q8_block_m16"] = {"us": 1e3 * ms, "decoded_GBps": 2 * weights / (ms * 1e-3) / 1e9,
                            "stream_GBps": qbytes / (ms * 1e-3) / 1e9, "frac_hbm": qbytes / (ms * 1e-3) / 1e9 / hbm}
 
+    # ---- the LM head (151936 x 5120), W12-encoded once
     V, K = LMHEAD
-    W = torch.empty((V, K), dtype=torch.int16, device="cuda")
+    W = torch.empty((V, K), dtype=torch.int16, device=dev)
     synth.weights_dev(0, 0, 9, W)
     H = w12.encode(W)
     del W
     torch.cuda.empty_cache()
-    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
-    synth.activations_dev(1, 0, 9, x)
-    import numpy as np
-    parent = torch.from_numpy(synth.tree(2, 0, 1, M)).cuda()
-    draft = torch.from_numpy(synth.drafts(3, 0, 1, M, V)).cuda()
-    ws2 = w12.Workspace()
-    ms = timed(lambda: w12.w12_lmhead_verify(x, H, parent, draft, ws=ws2), steps)
+    ws2 = w12.Workspace(dev)
+
+    def head_case(Mh, xseed_tensor, n_req, nodes):
+        x = torch.empty((Mh, K), dtype=torch.int16, device=dev)
+        synth.activations_dev(1, 0, xseed_tensor, x)
+        parent = np.concatenate([synth.tree(2, r, nodes, nodes) for r in range(n_req)]).astype(np.int32)
+        draft = np.concatenate([synth.drafts(3, r, nodes, nodes, V) for r in range(n_req)]).astype(np.int32)
+        offsets = None if n_req == 1 else torch.from_numpy(np.arange(0, Mh + 1, nodes, dtype=np.int32)).to(dev)
+        p, d = torch.from_numpy(parent).to(dev), torch.from_numpy(draft).to(dev)
+        fn = lambda: w12.w12_lmhead_verify(x, H, p, d, req_offsets=offsets, ws=ws2)
+        return x, fn
+
+    x16, fn = head_case(M, 9, 1, M)
+    ms = timed_ms(torch, fn, steps)
     hb = H.stream_bytes() + 2 * M * K
     out["lmhead_verify_m16"] = {"us": 1e3 * ms, "decoded_GBps": 2 * V * K / (ms * 1e-3) / 1e9,
                                 "stream_GBps": hb / (ms * 1e-3) / 1e9, "frac_hbm": hb / (ms * 1e-3) / 1e9 / hbm}
+
+    # ---- the 64-layer stack at M = 32: exact pass, Q8 pass, then the head + 32-node tree
+    if not args.no_stack:
+        Ms, layers = 32, 64
+        stack = [encode_block(w12, synth, torch, layer) for layer in range(layers)]
+        xs32, ys32 = [], []
+        for tensor, (_, A) in enumerate(stack[0]):
+            x = torch.empty((Ms, A.K), dtype=torch.int16, device=dev)
+            synth.activations_dev(1, 0, tensor, x)
+            xs32.append(x)
+            ys32.append(torch.empty((Ms, A.N), dtype=torch.float32, device=dev))
+        ws3 = w12.Workspace(dev)
+        ws3.get(max(w12.gemm_workspace_size(Ms, A.N, A.K) for _, A in stack[0]))
+
+        def pass_(q8):
+            f = w12.w12_gemm_q8 if q8 else w12.w12_gemm
+            for blk in stack:
+                for (_, A), x, y in zip(blk, xs32, ys32):
+                    f(x, A, y=y, ws=ws3)
+
+        n_pass = max(3, steps // 10)
+        w_stack = sum(A.N * A.K for blk in stack for _, A in blk)
+        stored = sum(A.stored_bytes() for blk in stack for _, A in blk)
+        n_esc = sum(A.n_esc for blk in stack for _, A in blk)
+        row = {}
+        for q8 in (False, True):
+            ms = timed_ms(torch, lambda: pass_(q8), n_pass, warm=1)
+            sb = sum(gemm_bytes(A, Ms, q8) for blk in stack for _, A in blk)
+            row["q8" if q8 else "exact"] = {
+                "ms_per_pass": ms, "us_per_layer": 1e3 * ms / layers,
+                "decoded_GBps": 2 * w_stack / (ms * 1e-3) / 1e9, "stream_GBps": sb / (ms * 1e-3) / 1e9,
+                "frac_hbm": sb / (ms * 1e-3) / 1e9 / hbm}
+        out["stack64_m32"] = {"layers": layers, "weights": w_stack, "stored_bytes": stored,
+                              "bits_per_weight": 8.0 * stored / w_stack, "escape_fraction": n_esc / w_stack,
+                              **row}
+        # config 3: Q8 stack pass, then the W12 head with argmax + 32-node tree acceptance
+        x32, fn32 = head_case(Ms, 9, 1, Ms)
+        ms_head = timed_ms(torch, fn32, steps)
+        ms_q = row["q8"]["ms_per_pass"]
+        # Q-vs-exact top-1 agreement of the head: the 32 rows plus 1024 more seeded rows
+        xa = torch.empty((1024, K), dtype=torch.int16, device=dev)
+        synth.activations_dev(1, 0, 11, xa)
+        agree, total = 0, 0
+        for xx in (x32, xa):
+            te = w12.w12_lmhead_argmax(xx, H, ws=ws2)
+            tq = w12.w12_lmhead_argmax(xx, H, q8=True, ws=ws2)
+            agree += int((te == tq).sum())
+            total += xx.shape[0]
+        out["q8_stack64_m32_head_tree32"] = {
+            "q8_pass_ms": ms_q, "head_verify_us": 1e3 * ms_head, "total_ms": ms_q + ms_head,
+            "q_vs_exact_top1_agreement": agree / total, "agreement_rows": total}
+        del stack
+        torch.cuda.empty_cache()
+
+    # ---- M = 192: the block and the head, 24 requests x 8 nodes
+    Mb = 192
+    xb, yb = [], []
+    for tensor, (_, A) in enumerate(mats):
+        x = torch.empty((Mb, A.K), dtype=torch.int16, device=dev)
+        synth.activations_dev(1, 1, tensor, x)
+        xb.append(x)
+        yb.append(torch.empty((Mb, A.N), dtype=torch.float32, device=dev))
+    ws4 = w12.Workspace(dev)
+    ws4.get(max(w12.gemm_workspace_size(Mb, A.N, A.K) for _, A in mats))
+
+    def blk192():
+        for (_, A), x, y in zip(mats, xb, yb):
+            w12.w12_gemm(x, A, y=y, ws=ws4)
+
+    ms_b = timed_ms(torch, blk192, steps)
+    x192, fn192 = head_case(Mb, 10, 24, 8)
+    ms_h = timed_ms(torch, fn192, steps)
+    tf, tf_kind = bf16_peak()
+    b_bytes = sum(gemm_bytes(A, Mb) for _, A in mats)
+    h_bytes = H.stream_bytes() + 2 * Mb * K
+    b_flops = sum(2.0 * Mb * A.N * A.K for _, A in mats)
+    h_flops = 2.0 * Mb * V * K
+
+    def roof(ms, nbytes, flops):
+        t_hbm = nbytes / (hbm * 1e9) * 1e3
+        t_tc = flops / (tf * 1e12) * 1e3
+        return {"us": 1e3 * ms, "hbm_floor_us": 1e3 * t_hbm, "tensor_floor_us": 1e3 * t_tc,
+                "frac_of_binding_roofline": max(t_hbm, t_tc) / ms,
+                "binding": "hbm" if t_hbm >= t_tc else "tensor",
+                "tflops": flops / (ms * 1e-3) / 1e12, "stream_GBps": nbytes / (ms * 1e-3) / 1e9}
+
+    out["block_head_m192_24trees"] = {"block": roof(ms_b, b_bytes, b_flops), "head_verify": roof(ms_h, h_bytes, h_flops),
+                                      "total_us": 1e3 * (ms_b + ms_h), "tensor_peak_tflops": tf,
+                                      "tensor_peak_kind": tf_kind}
     del H
     torch.cuda.empty_cache()
     return out

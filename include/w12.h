@@ -53,7 +53,9 @@
  *  - base: N bytes, the window base of each channel.
  *  - esc_tile_ptr: RT*KC+1 u32, exclusive prefix of escape counts per tile.
  *  - esc: n_esc u32 entries, grouped by tile and sorted by (channel, column)
- *         within a tile: raw bf16 | (column-in-chunk) << 16 | (channel-in-tile) << 22.
+ *         within a tile: raw bf16 | slot << 16, where slot is the byte offset of
+ *         (channel-in-tile r, column-in-chunk c) in the tile's decoded 32x64 bf16
+ *         image with a 128-byte swizzle: r*128 + ((c/8 XOR r%8) * 16) + (c%8)*2.
  *         The allocation holds ceil(n_esc/4)*4 entries (at least 4): the GEMM
  *         copies escapes in aligned 16-byte runs.
  *  hi, lo and esc must be 16-byte aligned (cudaMalloc gives 256).

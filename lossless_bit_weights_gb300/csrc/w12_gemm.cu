@@ -190,10 +190,10 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target) {
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Rendezvous of a decode group's four warps on an mbarrier, bounded.
+// Rendezvous of a decode group's four warps (all 128 threads arrive) on an mbarrier, bounded.
 __device__ __forceinline__ bool epi_sync(uint32_t bar, uint32_t& phase, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
+  (void)lane;
+  mbar_arrive(bar);
   const bool ok = warp_wait(bar, phase & 1u);
   ++phase;
   return ok;
@@ -254,19 +254,19 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
     misc[15] = 0u;
     for (int i = 0; i < S; ++i) {
       mbar_init(rec_full0 + 8 * i, 1);
-      mbar_init(rec_empty0 + 8 * i, kBlockTiles);
+      mbar_init(rec_empty0 + 8 * i, kBlockTiles * 32);
     }
     for (int i = 0; i < SX; ++i) {
       mbar_init(x_full0 + 8 * i, 1);
       mbar_init(x_empty0 + 8 * i, 1);
     }
     for (int i = 0; i < kTcGroups; ++i) {
-      mbar_init(a_full0 + 8 * i, kBlockTiles);
+      mbar_init(a_full0 + 8 * i, kBlockTiles * 32);
       mbar_init(a_empty0 + 8 * i, 1);
-      mbar_init(epi0 + 8 * i, kBlockTiles);
+      mbar_init(epi0 + 8 * i, kBlockTiles * 32);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kBlockTiles);
+    mbar_init(acc_empty, kBlockTiles * 32);
     mbar_init(mma_done, 1);
     mbar_init_fence();
   }
@@ -457,9 +457,8 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
           ent = e - e0 < (uint32_t)kEscRun ? reinterpret_cast<const uint32_t*>(rec + P::kOffEsc)[e - e0]
                                            : __ldg(a.esc + e);
         }
-        // the record stage can be refilled now
-        __syncwarp();
-        if (lane == 0) mbar_arrive(rec_empty0 + 8 * s);
+        // the record stage can be refilled now (every thread arrives once its own loads are done)
+        mbar_arrive(rec_empty0 + 8 * s);
         // Decode into registers, then wait until the group's A buffer is free (the MMA of
         // its previous unit has finished), so that the decode overlaps the tensor cores'
         // work on that unit.
@@ -477,23 +476,16 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
           *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) =
               make_uint4(pr[q][4], pr[q][5], pr[q][6], pr[q][7]);
         }
-        __syncwarp();
-        if ((uint32_t)lane < cnt) {
-          const int er = esc_row(ent), ek = esc_col(ent);
-          *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
-              (uint16_t)esc_raw(ent);
-        }
+        __syncwarp();  // the decoded stores of all lanes land before any escape overwrites a slot
+        if ((uint32_t)lane < cnt) *reinterpret_cast<uint16_t*>(atp + esc_slot(ent)) = (uint16_t)esc_raw(ent);
         if (cnt > 32u) {
           for (uint32_t e = ta + 32 + lane; e < tb; e += 32) {
             const uint32_t en = __ldg(a.esc + e);
-            const int er = esc_row(en), ek = esc_col(en);
-            *reinterpret_cast<uint16_t*>(atp + er * 128 + (((ek >> 3) ^ (er & 7)) << 4) + (ek & 7) * 2) =
-                (uint16_t)esc_raw(en);
+            *reinterpret_cast<uint16_t*>(atp + esc_slot(en)) = (uint16_t)esc_raw(en);
           }
         }
-        fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full);
+        fence_proxy_async_smem();  // this thread's generic-proxy stores -> tensor-core reads
+        mbar_arrive(a_full);
         ++mine;
       }
       if (kc == KC - 1 || j == nun - 1) {
@@ -522,11 +514,8 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
             emit_cols<EPI>(a, rt, lane, c0, v);
           }
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(acc_empty);
-            atomicAdd(misc + 15, 1u);
-          }
+          mbar_arrive(acc_empty);
+          if (lane == 0) atomicAdd(misc + 15, 1u);
         } else {
           const int64_t cf = cta_of_unit((int64_t)rb * KC, a.G, a.T);
           const int64_t cl = cta_of_unit((int64_t)(rb + 1) * KC - 1, a.G, a.T);
@@ -542,11 +531,8 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
               __stcg(slot + (c0 / 4 + i) * 32 + lane, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
           }
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(acc_empty);
-            atomicAdd(misc + 15, 1u);
-          }
+          mbar_arrive(acc_empty);
+          if (lane == 0) atomicAdd(misc + 15, 1u);
           __threadfence();
           if (!epi_sync(epi_bar, epi_phase, lane)) {
             bail = true;

@@ -50,12 +50,21 @@ __host__ __device__ inline int lo_bit(int r, int kk) {
   return (q * 256 + (4 * g + t) * 8) * 8 + 32 * (p >> 2) + 4 * (p & 3) + 16 * (j & 1);
 }
 
-// Escape entry of the device layout.
-__host__ __device__ inline uint32_t esc_entry(int rr, int kk, uint32_t raw) {
-  return raw | ((uint32_t)kk << 16) | ((uint32_t)rr << 22);
+// Escape entry of the device layout: raw bf16 | slot << 16, where slot is the
+// byte offset of (channel-in-tile rr, column-in-chunk kk) in the tile's decoded
+// 32x64 bf16 image with the 128-byte swizzle the GEMM's A operand uses: row rr
+// at rr*128, 16-byte chunk kk/8 stored at chunk (kk/8) ^ (rr%8).  The GEMM
+// patches an escape with one 2-byte store at that offset.
+__host__ __device__ inline uint32_t esc_slot_of(int rr, int kk) {
+  return (uint32_t)(rr * 128 + ((((kk >> 3) ^ (rr & 7)) & 7) << 4) + (kk & 7) * 2);
 }
-__host__ __device__ inline int esc_row(uint32_t e) { return (int)(e >> 22); }
-__host__ __device__ inline int esc_col(uint32_t e) { return (int)((e >> 16) & 63u); }
+__host__ __device__ inline uint32_t esc_entry(int rr, int kk, uint32_t raw) { return raw | (esc_slot_of(rr, kk) << 16); }
+__host__ __device__ inline uint32_t esc_slot(uint32_t e) { return e >> 16; }
+__host__ __device__ inline int esc_row(uint32_t e) { return (int)(e >> 23); }
+__host__ __device__ inline int esc_col(uint32_t e) {
+  const uint32_t off = e >> 16, rr = off >> 7;
+  return (int)(((((off >> 4) & 7u) ^ (rr & 7u)) << 3) | ((off >> 1) & 7u));
+}
 __host__ __device__ inline uint32_t esc_raw(uint32_t e) { return e & 0xFFFFu; }
 
 // ---------------------------------------------------------------- status

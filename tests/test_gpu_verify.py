@@ -121,15 +121,101 @@ def test_lmhead_tiny(w12, q8):
     check_paths(pl, pn, bo, tok, parent, draft, np.array([0, 8]))
 
 
-def test_lmhead_full_size_m32(w12):
-    """151936 x 5120 head at M = 32: full fp64 oracle logits on the host."""
-    V, K, M = 151936, 5120, 32
+HEAD = (151936, 5120)   # the LM head of the 27B-class configs: vocab x hidden
+
+
+@pytest.fixture(scope="module")
+def head(w12):
+    """The 151936 x 5120 head, W12-encoded on the device (seed 0, tensor 9)."""
+    V, K = HEAD
     Wd = device_weights(0, 0, 9, V, K)
     A = w12.encode(Wd)
     del Wd
-    x = synth.activations(1, 0, 9, M, K)
-    tok = w12.w12_lmhead_argmax(to_dev16(x), A).cpu().numpy()
+    torch.cuda.empty_cache()
+    return A
+
+
+@pytest.fixture(scope="module")
+def head_host():
+    """The same head's bf16 bits generated on the host, and its oracle encoding."""
+    V, K = HEAD
     Wh = synth.weights(0, 0, 9, V, K)
+    return Wh, oracle.encode(Wh)
+
+
+def planted_tree(seed_layer, n, V, tok, rng, p_plant=0.5):
+    """A random tree (parent of node i uniform over 0..i-1) with uniform drafts over
+    the vocab, where each node's draft is set to its parent's target token with
+    probability p_plant, so that acceptance is exercised."""
+    parent = synth.tree(2, seed_layer, n, n)
+    draft = synth.drafts(3, seed_layer, n, n, V)
+    for i in range(1, n):
+        if rng.random() < p_plant:
+            draft[i] = tok[parent[i]]
+    return parent, draft
+
+
+def test_lmhead_full_size_m32(w12, head, head_host):
+    """151936 x 5120 head at M = 32: fp64 oracle logits on the host for every row, then
+    greedy acceptance on a 32-node tree from the fused verify call."""
+    V, K = HEAD
+    M = 32
+    Wh, _ = head_host
+    x = synth.activations(1, 0, 9, M, K)
+    tok = w12.w12_lmhead_argmax(to_dev16(x), head).cpu().numpy()
     y64 = oracle.gemm(x, Wh, with_bound=False)
     ties = argmax_check(tok, y64)
     assert ties <= 1
+    rng = np.random.default_rng(32)
+    for plant in (0.0, 0.5, 1.0):   # the literal uniform drafts, then planted ones
+        parent, draft = planted_tree(32, M, V, tok, rng, plant)
+        t2, pl, pn, bo = w12.w12_lmhead_verify(to_dev16(x), head, i32(parent), i32(draft))
+        assert np.array_equal(t2.cpu().numpy(), tok)
+        check_paths(pl, pn, bo, tok, parent, draft, np.array([0, M]))
+
+
+def test_lmhead_q8_full_size_m32_and_agreement(w12, head, head_host):
+    """The 8-bit-view head at M = 32 against the oracle's Q8 logits, and the Q-vs-exact
+    top-1 agreement: the rate the GPU reports equals the oracle's on the same rows
+    (rows whose oracle top-2 gap is below the tie bound are left out of the comparison)."""
+    V, K = HEAD
+    M = 32
+    Wh, enc = head_host
+    x = synth.activations(1, 0, 9, M, K)
+    xd = to_dev16(x)
+    tq = w12.w12_lmhead_argmax(xd, head, q8=True).cpu().numpy()
+    te = w12.w12_lmhead_argmax(xd, head).cpu().numpy()
+    yq = oracle.gemm(x, oracle.decode_q8(enc), with_bound=False)
+    ye = oracle.gemm(x, Wh, with_bound=False)
+    assert argmax_check(tq, yq) <= 1
+    iq, gq = oracle.argmax(yq)
+    ie, ge = oracle.argmax(ye)
+    clear = (gq >= TIE) & (ge >= TIE)
+    assert clear.sum() >= M - 2
+    assert np.array_equal((tq == te)[clear], (iq == ie)[clear])
+
+
+def test_lmhead_m192_24_trees(w12, head, head_host):
+    """24 requests x 8 tree nodes = 192 rows through the head in one call with per-request
+    acceptance: the argmax of 16 sampled rows against fp64 oracle logits, and every
+    request's path and bonus bit-exact against the oracle on the GPU's tokens."""
+    V, K = HEAD
+    M, n_req, nodes = 192, 24, 8
+    Wh, _ = head_host
+    x = synth.activations(1, 0, 10, M, K)
+    tok = w12.w12_lmhead_argmax(to_dev16(x), head).cpu().numpy()
+    rows = np.sort(np.random.default_rng(192).choice(M, 16, replace=False))
+    y64 = oracle.gemm(x[rows], Wh, with_bound=False)
+    assert argmax_check(tok[rows], y64) <= 1
+    rng = np.random.default_rng(24)
+    parents, drafts = [], []
+    for r in range(n_req):
+        p, d = planted_tree(100 + r, nodes, V, tok[r * nodes:(r + 1) * nodes], rng)
+        parents.append(p), drafts.append(d)
+    parent = np.concatenate(parents).astype(np.int32)
+    draft = np.concatenate(drafts).astype(np.int32)
+    offsets = np.arange(0, M + 1, nodes, dtype=np.int32)
+    t2, pl, pn, bo = w12.w12_lmhead_verify(to_dev16(x), head, i32(parent), i32(draft), req_offsets=i32(offsets))
+    assert np.array_equal(t2.cpu().numpy(), tok)
+    check_paths(pl, pn, bo, tok, parent, draft, offsets)
+    assert (pl.cpu().numpy() > 0).sum() >= 1   # the planted drafts accept somewhere
