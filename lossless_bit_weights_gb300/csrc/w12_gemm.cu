@@ -102,7 +102,10 @@ template <int NT, bool Q8>
 struct TcPlan {
   static constexpr int kBlocksPerSM = NT <= 32 ? 2 : 1;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
-  static constexpr int kXStages = NT <= 64 ? 4 : 2;
+#ifndef W12_TC_XSTAGES_BIG
+#define W12_TC_XSTAGES_BIG 2
+#endif
+  static constexpr int kXStages = NT <= 64 ? 4 : W12_TC_XSTAGES_BIG;
   static constexpr int kHi = kBlockTiles * kHiTileBytes;
   static constexpr int kLo = Q8 ? 0 : kBlockTiles * kLoTileBytes;
   static constexpr int kOffLo = kHi;
@@ -285,33 +288,30 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
   if (warp == kTcProducer) {
     // ---------------------------------------------------------------- weight records
     const uint64_t pol_w = policy_evict_first();
-    // tile_ptr[wb .. wb+95] held across the lanes in three registers; the third
-    // is loaded 8 units before any shuffle reads it.
-    int64_t wb = 4 * u0;
-    const int64_t TT = 4 * a.T;
-    uint32_t w0 = wb + lane <= TT ? __ldg(a.tile_ptr + wb + lane) : 0u;
-    uint32_t w1 = wb + 32 + lane <= TT ? __ldg(a.tile_ptr + wb + 32 + lane) : 0u;
-    uint32_t w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
+    // tile_ptr[4u0 + wr .. 4u0 + wr + 95] held across the lanes in three registers; the
+    // third is loaded 8 units before any shuffle reads it.
+    const uint32_t* tpw = a.tile_ptr + 4 * u0;
+    const int64_t TT = 4 * (a.T - u0);  // entries left from tpw on (tile_ptr has 4T+1)
+    int wr = 0;
+    uint32_t w0 = lane <= TT ? __ldg(tpw + lane) : 0u;
+    uint32_t w1 = 32 + lane <= TT ? __ldg(tpw + 32 + lane) : 0u;
+    uint32_t w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
+    const uint8_t* hp = a.hi + u0 * P::kHi;
+    const uint8_t* lp = a.lo + u0 * (kBlockTiles * kLoTileBytes);
     int issued = 0, s = 0;
     uint32_t ph = 0;  // parity of the empty phase to wait for, once the ring has wrapped
     for (int j = 0; j < nun; ++j) {
-      const int64_t u = u0 + j;
-      if (j >= S) {
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(rec_empty0 + 8 * s, ph);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-          bail = true;
-          break;
-        }
+      if (j >= S && !warp_wait(rec_empty0 + 8 * s, ph)) {
+        bail = true;
+        break;
       }
-      if (4 * u - wb >= 32) {
+      if (4 * j - wr >= 32) {
         w0 = w1;
         w1 = w2;
-        wb += 32;
-        w2 = wb + 64 + lane <= TT ? __ldg(a.tile_ptr + wb + 64 + lane) : 0u;
+        wr += 32;
+        w2 = wr + 64 + lane <= TT ? __ldg(tpw + wr + 64 + lane) : 0u;
       }
-      const int d = (int)(4 * u - wb);
-      const int src = d + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4u + i]
+      const int src = 4 * j - wr + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4u + i]
       const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
       const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
       const uint32_t tpv = src < 32 ? v0 : v1;
@@ -321,17 +321,18 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
       if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
       const uint32_t esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
       uint8_t* rec = smem + P::kOffRec + s * P::kRec;
-      if (lane < 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = tpv;
-      if (lane == 5) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[5] = e0;
+      if (lane < 6) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = lane < 5 ? tpv : e0;
       __syncwarp();
       if (lane == 0) {
         const uint32_t full = rec_full0 + 8 * s;
         const uint32_t recs = sbase + P::kOffRec + s * P::kRec;
         mbar_arrive_expect_tx(full, P::kHi + P::kLo + esc_bytes);
-        bulk_g2s(recs, a.hi + u * P::kHi, P::kHi, full, pol_w);
-        if (!Q8) bulk_g2s(recs + P::kOffLo, a.lo + u * (kBlockTiles * kLoTileBytes), P::kLo, full, pol_w);
+        bulk_g2s(recs, hp, P::kHi, full, pol_w);
+        if (!Q8) bulk_g2s(recs + P::kOffLo, lp, P::kLo, full, pol_w);
         if (esc_bytes) bulk_g2s(recs + P::kOffEsc, a.esc + e0, esc_bytes, full, pol_w);
       }
+      hp += P::kHi;
+      lp += kBlockTiles * kLoTileBytes;
       issued = j + 1;
       if (++s == S) {
         s = 0;
@@ -373,32 +374,44 @@ __global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc<NT>();
-      int64_t kc = u0 % a.KC;
-      int seg = 0;
+      // Descriptors are built once: a K step of 16 adds 32 bytes (2 in the 16-byte address
+      // field) and an x stage adds kX bytes.  Shared addresses stay below 2^18, so the
+      // address field never carries into the neighbouring bits.
+      const uint64_t ad0 = umma_desc(sbase + P::kOffA), xd0 = umma_desc(sbase);
+      const int KC = (int)a.KC;
+      int kc = (int)(u0 % a.KC);
+      int seg = 0, s = 0, gi = 0;
+      uint32_t xph = 0, aph = 0;
       for (int j = 0; j < nun; ++j) {
-        const int s = j % SX, gi = j % kTcGroups;
         const bool first = (j == 0) || (kc == 0);
         if (first && j > 0 && !mbar_wait_bounded(acc_empty, (uint32_t)((seg - 1) & 1))) {
           bail = true;
           break;
         }
-        if (!mbar_wait_bounded(a_full0 + 8 * gi, (uint32_t)((j / kTcGroups) & 1)) ||
-            !mbar_wait_bounded(x_full0 + 8 * s, (uint32_t)((j / SX) & 1))) {
+        if (!mbar_wait_bounded(a_full0 + 8 * gi, aph) || !mbar_wait_bounded(x_full0 + 8 * s, xph)) {
           bail = true;
           break;
         }
         tc_fence_after();
-        const uint32_t abase = sbase + P::kOffA + gi * kABuf, xbase = sbase + s * P::kX;
+        const uint64_t ad = ad0 + (uint64_t)((gi * kABuf) >> 4), xd = xd0 + (uint64_t)((s * P::kX) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem, umma_desc(abase + ks * 32), umma_desc(xbase + ks * 32), idesc, (first && ks == 0) ? 0u : 1u);
+          umma_bf16(tmem, ad + 2 * ks, xd + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
         umma_commit(a_empty0 + 8 * gi);
         umma_commit(x_empty0 + 8 * s);
-        if ((kc + 1 == a.KC) || (j + 1 == nun)) {
+        if (kc + 1 == KC || j + 1 == nun) {
           umma_commit(acc_full);
           ++seg;
         }
-        if (++kc == a.KC) kc = 0;
+        if (++kc == KC) kc = 0;
+        if (++s == SX) {
+          s = 0;
+          xph ^= 1u;
+        }
+        if (++gi == kTcGroups) {
+          gi = 0;
+          aph ^= 1u;
+        }
       }
       // every MMA issued here has finished before TMEM is released
       umma_commit(mma_done);
@@ -654,7 +667,7 @@ struct LaunchShape {
   int nt, bpsm;
 };
 LaunchShape launch_shape(int64_t M) {
-  const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 192 ? 192 : 256;
   return {nt, nt <= 32 ? 2 : 1};
 }
 
@@ -750,6 +763,7 @@ int launch_nt(int nt, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s)
     case 32: return launch_tc<32, Q8, EPI>(map, a, s);
     case 64: return launch_tc<64, Q8, EPI>(map, a, s);
     case 128: return launch_tc<128, Q8, EPI>(map, a, s);
+    case 192: return launch_tc<192, Q8, EPI>(map, a, s);
     default: return launch_tc<256, Q8, EPI>(map, a, s);
   }
 }
