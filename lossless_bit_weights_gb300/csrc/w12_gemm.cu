@@ -92,15 +92,17 @@ __device__ __forceinline__ void tma_x(uint32_t dst, const CUtensorMap* map, int 
 // four groups a group has four unit-times for its own unit, so a record stage
 // is taken as soon as it lands and the whole shared memory of the SM serves
 // one deep ring.
-constexpr int kTcGroups = 2;
-constexpr int kTcDecoders = kTcGroups * kBlockTiles;
-constexpr int kTcProducer = kTcDecoders, kTcMma = kTcDecoders + 1, kTcX = kTcDecoders + 2;
-constexpr int kTcThreads = (kTcDecoders + 3) * 32;
 constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 block (16 KB, swizzled)
 
+// NT <= 32: two CTAs per SM; larger NT: one CTA per SM (its x stages are larger).  Two
+// decode groups per CTA in both cases (four groups at NT = 128/192 measured slower overall).
 template <int NT, bool Q8>
 struct TcPlan {
   static constexpr int kBlocksPerSM = NT <= 32 ? 2 : 1;
+  static constexpr int kGroups = 2;
+  static constexpr int kDecoders = kGroups * kBlockTiles;
+  static constexpr int kProducer = kDecoders, kMma = kDecoders + 1, kXWarp = kDecoders + 2;
+  static constexpr int kThreads = (kDecoders + 3) * 32;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
 #ifndef W12_TC_XSTAGES_BIG
 #define W12_TC_XSTAGES_BIG 2
@@ -113,17 +115,17 @@ struct TcPlan {
   static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
   static constexpr int kRec = kOffHdr + 32;
   static constexpr int kOffA = kXStages * kX;                 // one A buffer per decode group
-  static constexpr int kOffRec = kOffA + kTcGroups * kABuf;
+  static constexpr int kOffRec = kOffA + kGroups * kABuf;
   static constexpr int kBudget = (kBlocksPerSM == 2 ? 112 : 224) * 1024;
   static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
   // rec_full[S] rec_empty[S] x_full[SX] x_empty[SX] a_full[G] a_empty[G] epi[G] acc_full acc_empty mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kTcGroups + 3;
+  static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
-  static_assert(kStages >= 3 && kStages > kTcGroups, "record ring too shallow");
+  static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
   static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
 
@@ -232,10 +234,11 @@ __device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lan
 }
 
 template <int NT, bool Q8, int EPI>
-__global__ void __launch_bounds__(kTcThreads, TcPlan<NT, Q8>::kBlocksPerSM)
+__global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlocksPerSM)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
   using P = TcPlan<NT, Q8>;
-  constexpr int S = P::kStages, SX = P::kXStages;
+  constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups;
+  constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.x;
@@ -743,7 +746,7 @@ int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.G);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(TcPlan<NT, Q8>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
