@@ -65,6 +65,8 @@ def _L():
             lib.w12o_argmax.restype = None
             lib.w12o_accept.argtypes = [p, p, p, i32, p, p]
             lib.w12o_accept.restype = i32
+            lib.w12o_tlv_splice.argtypes = [i32, p, i32, p, p, p, i32, p, p, p]
+            lib.w12o_tlv_splice.restype = i32
             _lib = lib
         return _lib
 
@@ -188,3 +190,22 @@ def accept_batched(tok, parent, draft, offsets):
         a, b = int(offsets[r]), int(offsets[r + 1])
         res.append(accept(tok[a:b], parent[a:b], draft[a:b]))
     return res
+
+
+def tlv_splice(L, path, bonus, draft_q, sub_parent, sub_draft, n):
+    """The two-level-verification splice: the Q pass's accepted path (L, path, bonus)
+    on a tree with drafts draft_q, plus a subtree (sub_parent relative, -1 = under the
+    bonus node) cut to fill n nodes.  Returns (parent, draft, src) of the n-node tree,
+    src[i] = Q-pass row reused by node i, or -1 - r for new row r; None if invalid."""
+    path = _c(np.asarray(path if L >= 0 else [0]), np.int32)
+    draft_q = _c(draft_q, np.int32)
+    sub_parent = _c(np.asarray(sub_parent) if len(sub_parent) else np.zeros(1), np.int32)
+    sub_draft = _c(np.asarray(sub_draft) if len(sub_draft) else np.zeros(1), np.int32)
+    parent = np.empty(max(n, 1), np.int32)
+    draft = np.empty(max(n, 1), np.int32)
+    src = np.empty(max(n, 1), np.int32)
+    rc = int(_L().w12o_tlv_splice(int(L), _p(path), int(bonus), _p(draft_q), _p(sub_parent), _p(sub_draft), int(n),
+                                  _p(parent), _p(draft), _p(src)))
+    if rc != 0:
+        return None
+    return parent[:n].copy(), draft[:n].copy(), src[:n].copy()

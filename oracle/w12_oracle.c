@@ -229,3 +229,41 @@ int32_t w12o_accept(const int32_t* tok, const int32_t* parent, const int32_t* dr
   free(depth);
   return L;
 }
+
+/* Two-level verification splice (same page and section, TLV sentence: the Q
+ * pass over the 8-bit view finds the matching path and the bonus token in the
+ * draft tree; a subtree drafted again at its end is attached, and the 32-node
+ * tree is checked by one exact pass).  The page gives no numbering; the
+ * plainest one is used:
+ *   node 0..L      the Q pass's accepted path, in path order (node 0 = root);
+ *                  node i's parent is i-1 and its draft is draft_q[path[i]];
+ *   node L+1       the bonus node: parent L, draft = the Q pass's bonus token;
+ *   node L+2+j     subtree node j (j < n - L - 2): parent L+1 when
+ *                  sub_parent[j] < 0, else L+2+sub_parent[j]; draft sub_draft[j].
+ * src[i] is the Q-pass row node i reuses (path[i] for i <= L) or -1 - r for
+ * new row r (the bonus node takes new row 0, subtree node j new row j+1).
+ * Returns 0; returns -1 (and fills nothing) when the Q result is invalid
+ * (L < 0) or the path leaves no room for the bonus node (L + 2 > n), or when
+ * a subtree parent is not an earlier subtree node. */
+int32_t w12o_tlv_splice(int32_t L, const int32_t* path, int32_t bonus, const int32_t* draft_q,
+                        const int32_t* sub_parent, const int32_t* sub_draft, int32_t n, int32_t* parent,
+                        int32_t* draft, int32_t* src) {
+  if (L < 0 || L + 2 > n) return -1;
+  for (int32_t j = 0; j < n - L - 2; ++j)
+    if (sub_parent[j] >= j) return -1;
+  for (int32_t i = 0; i <= L; ++i) {
+    parent[i] = i - 1;
+    draft[i] = draft_q[path[i]];
+    src[i] = path[i];
+  }
+  parent[L + 1] = L;
+  draft[L + 1] = bonus;
+  src[L + 1] = -1;
+  for (int32_t j = 0; j < n - L - 2; ++j) {
+    const int32_t i = L + 2 + j;
+    parent[i] = sub_parent[j] < 0 ? L + 1 : L + 2 + sub_parent[j];
+    draft[i] = sub_draft[j];
+    src[i] = -1 - (j + 1);
+  }
+  return 0;
+}

@@ -4,7 +4,7 @@ The mutant is compiled on the CPU into a temporary library and the pin suite
 (test_oracle_pins.py) runs against it in a child process; the child must
 report a failure.  This shows the pins constrain every step of the oracle:
 window choice, record layout, planes, decode, the 8-bit view, the fp64 GEMM
-and its bound, argmax ties and tree acceptance.
+and its bound, argmax ties, tree acceptance and the two-level-verification splice.
 """
 import os
 import subprocess
@@ -37,6 +37,12 @@ MUTANTS = {
     "accept depth ties go high": ("if (acc[i] && depth[i] > depth[best]) best = i;",
                                   "if (acc[i] && depth[i] >= depth[best]) best = i;"),
     "bonus from parent": ("*bonus = tok[best];", "*bonus = tok[parent[best] < 0 ? 0 : parent[best]];"),
+    "splice bonus under the wrong node": ("  parent[L + 1] = L;", "  parent[L + 1] = L > 0 ? L - 1 : L;"),
+    "splice path drafts by position": ("    draft[i] = draft_q[path[i]];", "    draft[i] = draft_q[i];"),
+    "splice subtree parents not shifted": ("parent[i] = sub_parent[j] < 0 ? L + 1 : L + 2 + sub_parent[j];",
+                                           "parent[i] = sub_parent[j] < 0 ? L + 1 : L + 1 + sub_parent[j];"),
+    "splice new rows off by one": ("    src[i] = -1 - (j + 1);", "    src[i] = -1 - j;"),
+    "splice drops the bonus token": ("  draft[L + 1] = bonus;", "  draft[L + 1] = draft_q[path[L]];"),
 }
 
 

@@ -329,3 +329,73 @@ def test_accept_chain_all_match_gives_full_depth():
         draft = np.concatenate([[0], tok[:-1]]).astype(np.int32)
         L, path, bonus = oracle.accept(tok, parent, draft)
         assert L == n - 1 and path.tolist() == list(range(n)) and bonus == tok[-1]
+
+
+# ---------------------------------------------------------------- two-level verification splice
+
+def load_tlv_fixture():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "tlv_splice_cases.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        p = [t.strip() for t in line.split("|")]
+        ints = lambda t: [int(v) for v in t.split()] if t != "-" else None
+        cases.append(dict(name=p[0], L=int(p[1]), path=ints(p[2]) or [], bonus=int(p[3]), draft_q=ints(p[4]),
+                          sub_parent=ints(p[5]), sub_draft=ints(p[6]), n=int(p[7]), parent=ints(p[8]),
+                          draft=ints(p[9]), src=ints(p[10])))
+    return cases
+
+
+def test_golden_tlv_splices():
+    for c in load_tlv_fixture():
+        r = oracle.tlv_splice(c["L"], c["path"], c["bonus"], c["draft_q"], c["sub_parent"], c["sub_draft"], c["n"])
+        if c["parent"] is None:
+            assert r is None, c["name"]
+            continue
+        parent, draft, src = r
+        assert parent.tolist() == c["parent"], c["name"]
+        assert draft.tolist() == c["draft"], c["name"]
+        assert src.tolist() == c["src"], c["name"]
+
+
+def test_tlv_splice_keeps_the_q_path_accepted():
+    """Property of the splice itself: when the exact pass reproduces the Q pass's target
+    tokens on the reused rows, greedy acceptance on the spliced tree walks the whole Q
+    path and then the bonus node (L_exact >= L_q + 1, path prefix 0..L_q+1), whatever the
+    new rows' tokens.  Checked against the brute-force acceptance walk on random trees."""
+    import synth
+    rng = np.random.default_rng(21)
+    checked = 0
+    for t in range(400):
+        n1 = int(rng.integers(1, 32))
+        V = int(rng.integers(2, 6))
+        p1 = synth.tree(2, 50, t, n1)
+        tq = rng.integers(0, V, n1).astype(np.int32)
+        d1 = rng.integers(0, V, n1).astype(np.int32)
+        for i in range(1, n1):
+            if rng.random() < 0.6:
+                d1[i] = tq[p1[i]]
+        L, path, bonus = oracle.accept(tq, p1, d1)
+        n = 32
+        sp = np.array([-1 if j == 0 or rng.random() < 0.3 else int(rng.integers(0, j)) for j in range(n)], np.int32)
+        sd = rng.integers(0, V, n).astype(np.int32)
+        r = oracle.tlv_splice(L, path, bonus, d1, sp, sd, n)
+        if L + 2 > n:
+            assert r is None
+            continue
+        parent, draft, src = r
+        assert parent[0] == -1 and all(0 <= parent[i] < i for i in range(1, n))
+        assert sorted(src[src >= 0].tolist()) == sorted(path.tolist())
+        assert sorted((-1 - src[src < 0]).tolist()) == list(range(n - L - 1))
+        te = np.where(src >= 0, tq[np.maximum(src, 0)], rng.integers(0, V, n)).astype(np.int32)
+        L2, path2, _ = brute_force_accept(te, parent, draft)
+        assert L2 >= L + 1 and path2[:L + 2] == list(range(L + 2)), (t, L, L2, path2)
+        checked += 1
+    assert checked > 300
+
+
+def test_tlv_splice_rejects_invalid_input():
+    assert oracle.tlv_splice(-1, [], -1, [0], [-1], [0], 4) is None          # Q tree was invalid
+    assert oracle.tlv_splice(3, [0, 1, 2, 3], 5, [0, 1, 2, 3], [-1], [0], 4) is None   # no room for the bonus
+    assert oracle.tlv_splice(0, [0], 5, [0], [-1, 1], [0, 0], 4) is None      # subtree parent not earlier
