@@ -13,8 +13,10 @@ roofline of the GEMM kernel against the measured HBM copy bandwidth, the
 end-to-end figure through the public API with host buffers, the CPU oracle
 timed on a bounded sample, SM clocks sampled during the timed region, and
 (under "rows") the other hot-path rows timed in the same run: the Q8 pass over
-the same block and the 151936x5120 LM head with fused argmax and tree
-acceptance.
+the same block, the 151936x5120 LM head with fused argmax and tree acceptance,
+the 64-layer stack at M=32 (exact and Q8 passes, Q-vs-exact agreement), the
+two-level verification step (Q pass, splice, exact pass on 32-node trees) and
+the block and head at M=192 with 24 trees.
 
 --impl reference times the CPU oracle (the plain C reference of the method)
 on the same workload and metric, a bounded sample of rows per step.
@@ -554,6 +556,50 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
         out["q8_stack64_m32_head_tree32"] = {
             "q8_pass_ms": ms_q, "head_verify_us": 1e3 * ms_head, "total_ms": ms_q + ms_head,
             "q_vs_exact_top1_agreement": agree / total, "agreement_rows": total}
+
+        # two-level verification step: Q pass (8-bit view of the stack and the head) on a
+        # 32-node tree, splice of its accepted path + bonus + a subtree drafted again into a
+        # 32-node tree, exact pass (W12 stack and head) on that tree
+        n = Ms
+        rng = np.random.default_rng(7)
+        tq0 = w12.w12_lmhead_argmax(x32, H, q8=True, ws=ws2).cpu().numpy()
+        pq = synth.tree(2, 7, n, n)
+        dq = synth.drafts(3, 7, n, n, V)
+        for i in range(1, n):
+            if rng.random() < 0.7:
+                dq[i] = tq0[pq[i]]
+        sp = np.array([-1 if j == 0 or rng.random() < 0.3 else int(rng.integers(0, j)) for j in range(n - 2)], np.int32)
+        sd = synth.drafts(3, 8, n, n - 2, V)
+        pq_d, dq_d = torch.from_numpy(pq).to(dev), torch.from_numpy(dq).to(dev)
+        sp_d, sd_d = torch.from_numpy(sp).to(dev), torch.from_numpy(sd).to(dev)
+        xs_new = torch.empty((n - 1, K), dtype=torch.int16, device=dev)
+        synth.activations_dev(1, 0, 13, xs_new)
+        lens = {}
+
+        def tlv_step():
+            pass_(True)
+            _, pl, pn, bo = w12.w12_lmhead_verify(x32, H, pq_d, dq_d, q8=True, ws=ws2)
+            par, dr, _, xe = w12.tlv_splice(pl, pn, bo, dq_d, x32, sp_d, sd_d, xs_new, n)
+            pass_(False)
+            _, pl2, _, _ = w12.w12_lmhead_verify(xe, H, par, dr, ws=ws2)
+            lens["q"], lens["exact"] = pl, pl2
+
+        ms_tlv = timed_ms(torch, tlv_step, n_pass, warm=1)
+        # the splice alone, 20 calls captured in a CUDA graph (a call from Python takes longer
+        # to issue than the kernel takes to run)
+        pn0 = torch.zeros(n, dtype=torch.int32, device=dev)
+        bo0 = torch.zeros(1, dtype=torch.int32, device=dev)
+        splice = lambda: w12.tlv_splice(lens["q"], pn0, bo0, dq_d, x32, sp_d, sd_d, xs_new, n)
+        splice()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(20):
+                splice()
+        ms_splice = timed_ms(torch, graph.replay, 10) / 20
+        out["tlv_step_stack64_m32"] = {"ms_per_step": ms_tlv, "splice_us": 1e3 * ms_splice,
+                                       "q_path_len": int(lens["q"][0]), "exact_path_len": int(lens["exact"][0]),
+                                       "tree_nodes": n}
         del stack
         torch.cuda.empty_cache()
 

@@ -229,6 +229,31 @@ W12_API int tree_verify(const float* logits, int64_t M, int64_t V, const int32_t
                 const int32_t* req_offsets, int32_t n_req, int32_t* path_len, int32_t* path_nodes,
                 int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
 
+/* Two-level verification splice.  SpecPilot summary page (onedev.kr/papers/1654),
+ * section "What's different", TLV sentence: the Q pass over the 8-bit view finds the
+ * matching path and the bonus token in the draft tree; a subtree drafted again at the
+ * end of that path is attached and the resulting tree (32 nodes there) goes through one
+ * exact pass.  The page gives no numbering; this call uses:
+ *   node 0..L     the Q pass's accepted path in order: parent i-1, draft
+ *                 draft_q[path_nodes[i]], activation row x_q[path_nodes[i]];
+ *   node L+1      the bonus node: parent L, draft = *bonus, row x_sub[0];
+ *   node L+2+j    subtree node j (j < n-L-2): parent L+1 when sub_parent[j] < 0, else
+ *                 L+2+sub_parent[j]; draft sub_draft[j]; row x_sub[j+1].
+ * Inputs (device): path_len[1], path_nodes[>= L+1], bonus[1] as tree_verify writes them
+ * for one request; draft_q[n_q]; x_q[n_q*K] bf16 rows of the Q pass; sub_parent[n-2],
+ * sub_draft[n-2]; x_sub[(n-1)*K].  Outputs (device): parent_out[n], draft_out[n],
+ * src_out[n] (Q row reused by the node, or -1-r for x_sub row r), x_out[n*K], the exact
+ * pass's rows.  When the Q result is invalid (L < 0), the path leaves no room for the
+ * bonus node (L+2 > n), a path node is outside 0..n_q-1 or a subtree parent is not an
+ * earlier subtree node, every parent_out is -2 (tree_verify then reports the tree
+ * invalid), draft_out is -1 and x_out is zero.  The caller owns every buffer; the call is
+ * asynchronous on `stream` and allocates nothing.  Errors: W12_ERR_INVALID_ARG (null
+ * pointer), W12_ERR_SHAPE (n outside 2..2^20, K outside 1..65535). */
+W12_API int tlv_splice(const int32_t* path_len, const int32_t* path_nodes, const int32_t* bonus,
+                       const int32_t* draft_q, const uint16_t* x_q, int64_t n_q, const int32_t* sub_parent,
+                       const int32_t* sub_draft, const uint16_t* x_sub, int64_t n, int64_t K, int32_t* parent_out,
+                       int32_t* draft_out, int32_t* src_out, uint16_t* x_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,7 @@ SIGNATURES = [
     ("tree_verify_tokens", ctypes.c_int, [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P]),
     ("tree_verify_workspace_size", _SZ, [_I64]),
     ("tree_verify", ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
+    ("tlv_splice", ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P]),
 ]
 
 
@@ -315,3 +316,26 @@ def tree_verify(logits, parent, draft, req_offsets=None, stream=None):
                              _ptr(None if req_offsets is None else _i32(req_offsets)), n_req, _ptr(path_len),
                              _ptr(path_nodes), _ptr(bonus), _ptr(ws), ws.numel(), _stream(stream)))
     return path_len, path_nodes, bonus
+
+
+def tlv_splice(path_len, path_nodes, bonus, draft_q, x_q, sub_parent, sub_draft, x_sub, n: int, stream=None):
+    """Two-level-verification splice: the Q pass's accepted path (path_len, path_nodes,
+    bonus of one request, as tree_verify returns them) on a tree with drafts draft_q and
+    activation rows x_q [n_q, K], plus a subtree (sub_parent relative, -1 = under the bonus
+    node; sub_draft) with rows x_sub [n-1, K] (row 0 for the bonus node).  Returns
+    (parent, draft, src, x) of the n-node tree for the exact pass."""
+    x_q, x_sub = _bits16(x_q), _bits16(x_sub)
+    n_q, K = x_q.shape
+    if x_sub.shape != (n - 1, K):
+        raise ValueError(f"x_sub must be [{n - 1}, {K}]")
+    dev = x_q.device
+    parent = torch.empty(n, dtype=torch.int32, device=dev)
+    draft = torch.empty(n, dtype=torch.int32, device=dev)
+    src = torch.empty(n, dtype=torch.int32, device=dev)
+    x = torch.empty((n, K), dtype=x_q.dtype, device=dev)
+    sp = _i32(sub_parent) if n > 2 else None
+    sd = _i32(sub_draft) if n > 2 else None
+    _check(lib().tlv_splice(_ptr(_i32(path_len)), _ptr(_i32(path_nodes)), _ptr(_i32(bonus)), _ptr(_i32(draft_q)),
+                            _ptr(x_q), n_q, _ptr(sp), _ptr(sd), _ptr(x_sub), n, K, _ptr(parent), _ptr(draft),
+                            _ptr(src), _ptr(x), _stream(stream)))
+    return parent, draft, src, x

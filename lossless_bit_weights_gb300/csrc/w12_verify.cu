@@ -1,4 +1,5 @@
-// w12_verify.cu - greedy draft-tree acceptance and row argmax.
+// w12_verify.cu - greedy draft-tree acceptance, row argmax and the two-level
+// verification splice.
 //
 // The SpecPilot summary page (onedev.kr/papers/1654), section "What's
 // different", verifies a draft tree by taking the path whose tokens match the
@@ -110,6 +111,67 @@ int launch_accept(const int32_t* tok, const int32_t* parent, const int32_t* draf
   return W12_OK;
 }
 
+// Two-level verification splice, one block per node of the n-node output tree.  Every
+// block checks the inputs (O(n)), then fills its node: path nodes 0..L keep the Q pass's
+// path in order and reuse its rows, node L+1 is the bonus node, subtree node j is node
+// L+2+j.  An invalid Q result, a path with no room for the bonus node, a path node outside
+// the Q tree or a subtree parent that is not an earlier subtree node gives parent -2 on
+// every node (acceptance then reports the tree invalid) and zero rows.
+__global__ void __launch_bounds__(256) k_tlv_splice(const int32_t* __restrict__ path_len,
+                                                    const int32_t* __restrict__ path_nodes,
+                                                    const int32_t* __restrict__ bonus,
+                                                    const int32_t* __restrict__ draft_q,
+                                                    const uint16_t* __restrict__ x_q, int64_t n_q,
+                                                    const int32_t* __restrict__ sub_parent,
+                                                    const int32_t* __restrict__ sub_draft,
+                                                    const uint16_t* __restrict__ x_sub, int64_t n, int64_t K,
+                                                    int32_t* parent_out, int32_t* draft_out, int32_t* src_out,
+                                                    uint16_t* __restrict__ x_out) {
+  __shared__ int32_t s_src;
+  const int64_t i = blockIdx.x;
+  const int32_t L = *path_len;
+  bool ok = L >= 0 && (int64_t)L + 2 <= n;
+  if (ok) {  // the checks are spread over the block
+    for (int64_t k = threadIdx.x; k <= L; k += blockDim.x) ok = ok && path_nodes[k] >= 0 && path_nodes[k] < n_q;
+    for (int64_t j = threadIdx.x; j < n - L - 2; j += blockDim.x) ok = ok && sub_parent[j] < j;
+  }
+  ok = __syncthreads_and(ok) != 0;
+  if (threadIdx.x == 0) {
+    int32_t par = -2, dr = -1, src = -1 - (int32_t)n;  // invalid: no row
+    if (ok) {
+      if (i <= L) {
+        par = (int32_t)i - 1;
+        dr = draft_q[path_nodes[i]];
+        src = path_nodes[i];
+      } else if (i == L + 1) {
+        par = L;
+        dr = *bonus;
+        src = -1;
+      } else {
+        const int64_t j = i - L - 2;
+        par = sub_parent[j] < 0 ? L + 1 : L + 2 + sub_parent[j];
+        dr = sub_draft[j];
+        src = -1 - (int32_t)(j + 1);
+      }
+    }
+    parent_out[i] = par;
+    draft_out[i] = dr;
+    src_out[i] = src;
+    s_src = src;
+  }
+  __syncthreads();
+  const int32_t src = s_src;
+  const uint16_t* row = src >= 0 ? x_q + (int64_t)src * K : (-1 - src < n ? x_sub + (int64_t)(-1 - src) * K : nullptr);
+  uint16_t* out = x_out + i * K;
+  const bool vec = (K % 8) == 0 && (((uintptr_t)x_q | (uintptr_t)x_sub | (uintptr_t)x_out) & 15u) == 0;
+  if (vec) {
+    for (int64_t k = threadIdx.x; k < K / 8; k += blockDim.x)
+      reinterpret_cast<uint4*>(out)[k] = row ? reinterpret_cast<const uint4*>(row)[k] : make_uint4(0, 0, 0, 0);
+  } else {
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = row ? row[k] : (uint16_t)0;
+  }
+}
+
 }  // namespace
 }  // namespace w12
 
@@ -151,6 +213,23 @@ int w12_lmhead_verify(const uint16_t* x, int64_t M, const w12_matrix* head, int 
   st = lmhead_argmax_impl(x, M, head, tok, q8 != 0, ws, ws_bytes, s, "w12_lmhead_verify");
   if (st) return st;
   return launch_accept(tok, parent, draft, req_offsets, n_req, M, path_len, path_nodes, bonus, s);
+}
+
+int tlv_splice(const int32_t* path_len, const int32_t* path_nodes, const int32_t* bonus, const int32_t* draft_q,
+               const uint16_t* x_q, int64_t n_q, const int32_t* sub_parent, const int32_t* sub_draft,
+               const uint16_t* x_sub, int64_t n, int64_t K, int32_t* parent_out, int32_t* draft_out, int32_t* src_out,
+               uint16_t* x_out, void* stream) {
+  if (!path_len || !path_nodes || !bonus || !draft_q || !x_q || !x_sub || !parent_out || !draft_out || !src_out ||
+      !x_out || (n > 2 && (!sub_parent || !sub_draft)))
+    return fail(W12_ERR_INVALID_ARG, "tlv_splice: null pointer");
+  if (n < 2 || n > (1 << 20) || n_q < 1 || n_q > 0x7FFFFFFF || K < 1 || K > kMaxK)
+    return fail(W12_ERR_SHAPE, "tlv_splice: n=%lld (2..2^20), n_q=%lld, K=%lld out of range", (long long)n,
+                (long long)n_q, (long long)K);
+  k_tlv_splice<<<(unsigned)n, 256, 0, (cudaStream_t)stream>>>(path_len, path_nodes, bonus, draft_q, x_q, n_q, sub_parent,
+                                                              sub_draft, x_sub, n, K, parent_out, draft_out, src_out,
+                                                              x_out);
+  W12_LAUNCH_CHECK("tlv_splice kernel");
+  return W12_OK;
 }
 
 }  // extern "C"

@@ -219,3 +219,34 @@ def test_lmhead_m192_24_trees(w12, head, head_host):
     assert np.array_equal(t2.cpu().numpy(), tok)
     check_paths(pl, pn, bo, tok, parent, draft, offsets)
     assert (pl.cpu().numpy() > 0).sum() >= 1   # the planted drafts accept somewhere
+
+
+def test_tlv_step_full_head(w12, head, head_host):
+    """The two-level verification step on the 151936 x 5120 head: a 32-node Q tree through
+    the 8-bit view, splice into a 32-node exact tree (subtree drafted again, planted to the
+    Q tokens half the time), exact pass; every argmax against fp64 oracle logits and the
+    final path bit-exact on the GPU's tokens."""
+    V, K = HEAD
+    n = 32
+    Wh, enc = head_host
+    rng = np.random.default_rng(33)
+    xq = synth.activations(1, 0, 12, n, K)
+    xs = synth.activations(1, 0, 13, n - 1, K)
+    tq = w12.w12_lmhead_argmax(to_dev16(xq), head, q8=True).cpu().numpy()
+    parent, draft = planted_tree(33, n, V, tq, rng, 0.7)
+    sp = np.array([-1 if j == 0 or rng.random() < 0.3 else int(rng.integers(0, j)) for j in range(n - 2)], np.int32)
+    sd = synth.drafts(3, 1, 33, n - 2, V)
+    t_q, pl, pn, bo = w12.w12_lmhead_verify(to_dev16(xq), head, i32(parent), i32(draft), q8=True)
+    assert np.array_equal(t_q.cpu().numpy(), tq)
+    assert argmax_check(tq, oracle.gemm(xq, oracle.decode_q8(enc), with_bound=False)) <= 1
+    check_paths(pl, pn, bo, tq, parent, draft, np.array([0, n]))
+    par, dr, src, x = w12.tlv_splice(pl, pn, bo, i32(draft), to_dev16(xq), i32(sp), i32(sd), to_dev16(xs), n)
+    L, path, bonus = oracle.accept(tq, parent, draft)
+    ref = oracle.tlv_splice(L, path, bonus, draft, sp, sd, n)
+    assert ref is not None and np.array_equal(par.cpu().numpy(), ref[0]) and np.array_equal(dr.cpu().numpy(), ref[1])
+    te, pl2, pn2, bo2 = w12.w12_lmhead_verify(x, head, par, dr)
+    xe = np.where(ref[2][:, None] >= 0, xq[np.maximum(ref[2], 0)], xs[np.clip(-1 - ref[2], 0, n - 2)])
+    te = te.cpu().numpy()
+    assert argmax_check(te, oracle.gemm(xe, Wh, with_bound=False)) <= 1
+    check_paths(pl2, pn2, bo2, te, ref[0], ref[1], np.array([0, n]))
+    assert int(pl2[0]) >= 0
