@@ -102,7 +102,15 @@ struct TcPlan {
   static constexpr int kGroups = 2;
   static constexpr int kDecoders = kGroups * kBlockTiles;
   static constexpr int kProducer = kDecoders, kMma = kDecoders + 1, kXWarp = kDecoders + 2;
-  static constexpr int kThreads = (kDecoders + 3) * 32;
+  static constexpr int kThreads = (kDecoders + 3) * 32;  // one pipeline
+  // For NT <= 32 two pipelines (each a full producer / decode / MMA set on its own unit
+  // range, shared-memory region and TMEM columns) share one CTA per SM.  As two CTAs on an
+  // SM, the older one's warps were favoured by the scheduler and it finished its equal
+  // share ~6 us sooner on gate/up (a launch ends with the slower one); as two pipelines of
+  // one CTA they finish together on average.
+  static constexpr int kPipes = NT <= 32 ? 2 : 1;
+  static constexpr int kCtaThreads = kPipes * kThreads;
+  static constexpr int kCtasPerSM = NT <= 32 ? 2 / kPipes : 1;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
 #ifndef W12_TC_XSTAGES_BIG
 #define W12_TC_XSTAGES_BIG 2
@@ -124,9 +132,11 @@ struct TcPlan {
   static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kPipeBytes = (kBytes + 1023) / 1024 * 1024;
+  static constexpr int kCtaBytes = kPipes == 1 ? kBytes : kPipes * kPipeBytes;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
   static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
-  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
+  static_assert(kCtaBytes <= 227 * 1024, "shared memory plan too large");
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -234,15 +244,30 @@ __device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lan
 }
 
 template <int NT, bool Q8, int EPI>
-__global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlocksPerSM)
+__global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::kCtasPerSM)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
   using P = TcPlan<NT, Q8>;
   constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups;
   constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t b = blockIdx.x;
-  if (b >= a.G) return;
+  extern __shared__ __align__(1024) uint8_t smem_cta[];
+  const int lane = threadIdx.x & 31, gwarp = threadIdx.x >> 5;
+  // pipeline and the warp's role index inside it: the decode warps of pipeline p are
+  // warps 8p..8p+7 (groups stay aligned to TMEM lane quarters), then each pipeline's
+  // producer, MMA issuer and x loader
+  int pipe = 0, warp = gwarp;
+  if (P::kPipes == 2) {
+    constexpr int nd = P::kDecoders;
+    if (gwarp < 2 * nd) {
+      pipe = gwarp / nd;
+      warp = gwarp % nd;
+    } else {
+      pipe = (gwarp - 2 * nd) / 3;
+      warp = nd + (gwarp - 2 * nd) % 3;
+    }
+  }
+  const int64_t b = (int64_t)blockIdx.x * P::kPipes + pipe;  // the pipeline's place in the partition
+  const bool active = b < a.G;
+  uint8_t* smem = smem_cta + pipe * P::kPipeBytes;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + P::kOffBar;
   const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S, x_full0 = bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
@@ -250,13 +275,13 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlo
   const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
   // misc: [0] TMEM address, [1+g] stream-K flag of group g, [15] drains finished (four per segment)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
-  const int64_t u0 = b * a.T / a.G, u1 = (b + 1) * a.T / a.G;
+  const int64_t u0 = active ? b * a.T / a.G : 0, u1 = active ? (b + 1) * a.T / a.G : 0;
   const int nun = (int)(u1 - u0);
 
   // The next kernel on the stream may start as this one's CTAs retire (programmatic
   // dependent launch): its weight stream does not depend on this kernel's output.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) {
+  if (warp == 0 && lane == 0) {
     misc[15] = 0u;
     for (int i = 0; i < S; ++i) {
       mbar_init(rec_full0 + 8 * i, 1);
@@ -276,19 +301,23 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlo
     mbar_init(mma_done, 1);
     mbar_init_fence();
   }
-  if (warp == kTcMma) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sbase + P::kOffMisc),
-                 "n"(P::kTmemCols)
+  // one warp allocates the TMEM columns of every pipeline (address in pipeline 0's misc[0])
+  uint32_t* misc0 = reinterpret_cast<uint32_t*>(smem_cta + P::kOffMisc);
+  if (warp == kTcMma && pipe == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc0)),
+                 "n"(P::kPipes * P::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = misc[0];
+  const uint32_t tmem = misc0[0] + (uint32_t)(pipe * P::kTmemCols);
   bool bail = false;
 
-  if (warp == kTcProducer) {
+  if (!active) {
+    // a pipeline with no place in the partition goes straight to the teardown
+  } else if (warp == kTcProducer) {
     // ---------------------------------------------------------------- weight records
     const uint64_t pol_w = policy_evict_first();
     // tile_ptr[4u0 + wr .. 4u0 + wr + 95] held across the lanes in three registers; the
@@ -475,22 +504,19 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlo
         }
         // the record stage can be refilled now (every thread arrives once its own loads are done)
         mbar_arrive(rec_empty0 + 8 * s);
-        // Decode into registers, then wait until the group's A buffer is free (the MMA of
-        // its previous unit has finished), so that the decode overlaps the tensor cores'
-        // work on that unit.
-        uint32_t pr[4][8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr[q]);
+        // the group's A buffer is free once the MMA of its previous unit has finished (issued
+        // while the other group decoded, so this wait rarely blocks)
         if (mine > 0 && !warp_wait(a_empty, (uint32_t)((mine - 1) & 1))) {
           bail = true;
           break;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+          uint32_t pr[8];
+          decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr);
           uint8_t* row = atp + (8 * q + g) * 128;
-          *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[q][0], pr[q][1], pr[q][2], pr[q][3]);
-          *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) =
-              make_uint4(pr[q][4], pr[q][5], pr[q][6], pr[q][7]);
+          *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
         }
         __syncwarp();  // the decoded stores of all lanes land before any escape overwrites a slot
         if ((uint32_t)lane < cnt) *reinterpret_cast<uint16_t*>(atp + esc_slot(ent)) = (uint16_t)esc_raw(ent);
@@ -608,8 +634,9 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kThreads, TcPlan<NT, Q8>::kBlo
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kTcMma)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(P::kTmemCols) : "memory");
+  if (warp == kTcMma && pipe == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(misc0[0]), "n"(P::kPipes * P::kTmemCols)
+                 : "memory");
 }
 
 // Copy of x with row pitch ldx (a multiple of 8 elements), zero past K.
@@ -736,7 +763,8 @@ int make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K, int64_
 
 template <int NT, bool Q8, int EPI>
 int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  constexpr int smem = TcPlan<NT, Q8>::kBytes;
+  using P = TcPlan<NT, Q8>;
+  constexpr int smem = P::kCtaBytes;
   static int configured_for_device[64] = {0};
   int dev = 0;
   W12_CUDA_TRY(cudaGetDevice(&dev));
@@ -745,8 +773,8 @@ int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
     if (dev < 64) configured_for_device[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.G);
-  cfg.blockDim = dim3(TcPlan<NT, Q8>::kThreads);
+  cfg.gridDim = dim3((unsigned)((a.G + P::kPipes - 1) / P::kPipes));
+  cfg.blockDim = dim3(P::kCtaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
