@@ -189,6 +189,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity));
 }
 
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Waits (bounded, warp-uniform) until a shared-memory counter reaches target.
 __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target) {
   bool ok = true;
@@ -575,12 +581,14 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
           tc_fence_before();
           mbar_arrive(acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
-          __threadfence();
+          // The group's barrier orders every thread's slot stores before one thread's
+          // acquire-release increment of the block's counter, which publishes them at GPU
+          // scope; the last arriver's increment acquires every other CTA's.
           if (!epi_sync(epi_bar, epi_phase, lane)) {
             bail = true;
             break;
           }
-          if (tl == 0 && lane == 0) misc[1 + gi] = atomicAdd(a.counters + rb, 1u);
+          if (tl == 0 && lane == 0) misc[1 + gi] = atom_add_acq_rel(a.counters + rb, 1u);
           if (!epi_sync(epi_bar, epi_phase, lane)) {
             bail = true;
             break;
@@ -591,7 +599,6 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
             break;
           }
           if (emit) {
-            __threadfence();
             if (tl == 0 && lane == 0) a.counters[rb] = 0u;
 #pragma unroll 1
             for (int c0 = 0; c0 < NT; c0 += 16) {
