@@ -67,6 +67,8 @@ def _L():
             lib.w12o_accept.restype = i32
             lib.w12o_tlv_splice.argtypes = [i32, p, i32, p, p, p, i32, p, p, p]
             lib.w12o_tlv_splice.restype = i32
+            lib.w12o_budget_select.argtypes = [p, p, p, p, i32, i32, i32, p, p, p, p]
+            lib.w12o_budget_select.restype = i32
             _lib = lib
         return _lib
 
@@ -209,3 +211,25 @@ def tlv_splice(L, path, bonus, draft_q, sub_parent, sub_draft, n):
     if rc != 0:
         return None
     return parent[:n].copy(), draft[:n].copy(), src[:n].copy()
+
+
+def budget_select(parent, conf, draft, offsets, budget, per_request=False):
+    """Node budget over several candidate trees (parent relative to its request, conf a
+    float32 confidence per node): keeps the top `budget` nodes by path score (over all
+    requests, or per request).  Returns (parent, draft, src, offsets) of the kept trees,
+    or None for an invalid candidate tree."""
+    parent = _c(parent, np.int32)
+    conf = _c(conf, np.float32)
+    draft = _c(draft, np.int32)
+    offsets = _c(offsets, np.int32)
+    n_req = offsets.size - 1
+    C = int(offsets[-1])
+    po = np.empty(max(C, 1), np.int32)
+    do = np.empty(max(C, 1), np.int32)
+    so = np.empty(max(C, 1), np.int32)
+    oo = np.empty(n_req + 1, np.int32)
+    k = int(_L().w12o_budget_select(_p(parent), _p(conf), _p(draft), _p(offsets), n_req, int(budget), int(per_request),
+                                    _p(po), _p(do), _p(so), _p(oo)))
+    if k < 0:
+        return None
+    return po[:k].copy(), do[:k].copy(), so[:k].copy(), oo.copy()

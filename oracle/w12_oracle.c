@@ -267,3 +267,79 @@ int32_t w12o_tlv_splice(int32_t L, const int32_t* path, int32_t bonus, const int
   }
   return 0;
 }
+
+/* Node budget shared across requests (same page and section: for batching, one node
+ * budget shared by all requests, 192 nodes for 24 requests).  The page gives no
+ * selection rule; the plainest one is used.  Request r owns candidate nodes
+ * off[r]..off[r+1]-1 (parent relative to the request, -1 for its root, parent < index);
+ * node i has a draft confidence conf[i] in (0, 1].  Its path score is the float product
+ * of the confidences from the root to i, taken root first (score of a root = its own
+ * confidence).  Nodes are ranked by (score descending, depth ascending, index
+ * ascending) and the first `budget` are kept: over all requests when per_request is 0,
+ * within each request (budget nodes each) otherwise.  A child never outranks its parent,
+ * so the kept set is closed under ancestors, and when conf is a calibrated acceptance
+ * probability it maximises the expected number of accepted nodes.  The kept nodes of a
+ * request are renumbered in their original order; outputs are parent_out, draft_out and
+ * src_out (the candidate index) per kept node, requests one after another, and
+ * off_out[n_req+1].  Returns the number kept, or -1 for an invalid candidate tree. */
+int32_t w12o_budget_select(const int32_t* parent, const float* conf, const int32_t* draft, const int32_t* off,
+                           int32_t n_req, int32_t budget, int32_t per_request, int32_t* parent_out,
+                           int32_t* draft_out, int32_t* src_out, int32_t* off_out) {
+  const int32_t C = off[n_req];
+  float* score = (float*)malloc(sizeof(float) * (size_t)(C > 0 ? C : 1));
+  int32_t* depth = (int32_t*)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+  int32_t* req = (int32_t*)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+  int32_t* keep = (int32_t*)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+  int32_t* newidx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+  int32_t kept = 0;
+  for (int32_t r = 0; r < n_req && kept >= 0; ++r) {
+    if (off[r + 1] <= off[r] || parent[off[r]] != -1) kept = -1;
+    for (int32_t i = off[r]; i < off[r + 1] && kept >= 0; ++i) {
+      const int32_t p = parent[i];
+      req[i] = r;
+      if (i == off[r]) {
+        score[i] = conf[i];
+        depth[i] = 0;
+      } else if (p < 0 || p >= i - off[r]) {
+        kept = -1;
+      } else {
+        score[i] = score[off[r] + p] * conf[i];
+        depth[i] = depth[off[r] + p] + 1;
+      }
+    }
+  }
+  if (kept == 0) {
+    /* rank of node i = number of nodes that come before it in the order (among all
+     * nodes, or among its request's) */
+    for (int32_t i = 0; i < C; ++i) {
+      int32_t rank = 0;
+      for (int32_t j = 0; j < C; ++j) {
+        if (j == i || (per_request && req[j] != req[i])) continue;
+        const int before = score[j] > score[i] ||
+                           (score[j] == score[i] && (depth[j] < depth[i] || (depth[j] == depth[i] && j < i)));
+        rank += before;
+      }
+      keep[i] = rank < budget;
+    }
+    for (int32_t r = 0; r < n_req; ++r) {
+      off_out[r] = kept;
+      int32_t n = 0;
+      for (int32_t i = off[r]; i < off[r + 1]; ++i) {
+        if (!keep[i]) continue;
+        newidx[i] = n;
+        parent_out[kept + n] = i == off[r] ? -1 : newidx[off[r] + parent[i]];
+        draft_out[kept + n] = draft[i];
+        src_out[kept + n] = i;
+        ++n;
+      }
+      kept += n;
+    }
+    off_out[n_req] = kept;
+  }
+  free(score);
+  free(depth);
+  free(req);
+  free(keep);
+  free(newidx);
+  return kept;
+}

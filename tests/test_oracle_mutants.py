@@ -43,6 +43,14 @@ MUTANTS = {
                                            "parent[i] = sub_parent[j] < 0 ? L + 1 : L + 1 + sub_parent[j];"),
     "splice new rows off by one": ("    src[i] = -1 - (j + 1);", "    src[i] = -1 - j;"),
     "splice drops the bonus token": ("  draft[L + 1] = bonus;", "  draft[L + 1] = draft_q[path[L]];"),
+    "budget scores add": ("score[i] = score[off[r] + p] * conf[i];", "score[i] = score[off[r] + p] + conf[i];"),
+    "budget deeper first on ties": ("(depth[j] < depth[i] || (depth[j] == depth[i] && j < i))",
+                                    "(depth[j] > depth[i] || (depth[j] == depth[i] && j < i))"),
+    "budget per request ignored": ("if (j == i || (per_request && req[j] != req[i])) continue;",
+                                   "if (j == i) continue;"),
+    "budget parents not renumbered": ("parent_out[kept + n] = i == off[r] ? -1 : newidx[off[r] + parent[i]];",
+                                      "parent_out[kept + n] = i == off[r] ? -1 : parent[i];"),
+    "budget keeps one too many": ("      keep[i] = rank < budget;", "      keep[i] = rank <= budget;"),
 }
 
 

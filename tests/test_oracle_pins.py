@@ -399,3 +399,112 @@ def test_tlv_splice_rejects_invalid_input():
     assert oracle.tlv_splice(-1, [], -1, [0], [-1], [0], 4) is None          # Q tree was invalid
     assert oracle.tlv_splice(3, [0, 1, 2, 3], 5, [0, 1, 2, 3], [-1], [0], 4) is None   # no room for the bonus
     assert oracle.tlv_splice(0, [0], 5, [0], [-1, 1], [0, 0], 4) is None      # subtree parent not earlier
+
+
+# ---------------------------------------------------------------- node budget shared across requests
+
+def load_budget_fixture():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "budget_cases.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        p = [t.strip() for t in line.split("|")]
+        ints = lambda t: [int(v) for v in t.split()]
+        cases.append(dict(name=p[0], off=ints(p[1]), parent=ints(p[2]), conf=[float(v) for v in p[3].split()],
+                          budget=int(p[4]), per_request=bool(int(p[5])), parent_out=ints(p[6]), src_out=ints(p[7]),
+                          off_out=ints(p[8])))
+    return cases
+
+
+def test_golden_budget_selections():
+    for c in load_budget_fixture():
+        draft = list(range(100, 100 + len(c["parent"])))
+        po, do, so, oo = oracle.budget_select(c["parent"], np.array(c["conf"], np.float32), draft, c["off"],
+                                              c["budget"], c["per_request"])
+        assert po.tolist() == c["parent_out"], c["name"]
+        assert so.tolist() == c["src_out"], c["name"]
+        assert oo.tolist() == c["off_out"], c["name"]
+        assert do.tolist() == [draft[i] for i in c["src_out"]], c["name"]
+
+
+def random_forest(rng, n_req, max_nodes, one_prob=0.2):
+    parents, confs, offs = [], [], [0]
+    for r in range(n_req):
+        n = int(rng.integers(1, max_nodes + 1))
+        p = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+        c = rng.uniform(0.05, 1.0, n).astype(np.float32)
+        c[rng.random(n) < one_prob] = 1.0       # ties: whole paths of equal score
+        parents.append(p), confs.append(c), offs.append(offs[-1] + n)
+    return np.concatenate(parents), np.concatenate(confs), np.array(offs, np.int32)
+
+
+def path_scores(parent, conf, off):
+    """float32 product of the confidences from the root, root first (written out here
+    independently of the oracle)."""
+    score = np.zeros(conf.size, np.float32)
+    depth = np.zeros(conf.size, np.int32)
+    for r in range(off.size - 1):
+        for i in range(off[r], off[r + 1]):
+            if i == off[r]:
+                score[i], depth[i] = conf[i], 0
+            else:
+                p = off[r] + parent[i]
+                score[i] = np.float32(score[p] * conf[i])
+                depth[i] = depth[p] + 1
+    return score, depth
+
+
+def test_budget_is_the_best_ancestor_closed_set():
+    """Brute force on tiny forests: the kept set is closed under ancestors, has
+    min(budget, nodes) nodes, and its score sum is the largest over every ancestor-closed
+    set of that size; kept parents are renumbered onto kept ancestors."""
+    import itertools
+    rng = np.random.default_rng(31)
+    for t in range(250):
+        parent, conf, off = random_forest(rng, int(rng.integers(1, 4)), 5)
+        C = int(off[-1])
+        budget = int(rng.integers(1, C + 2))
+        draft = np.arange(C, dtype=np.int32)
+        po, do, so, oo = oracle.budget_select(parent, conf, draft, off, budget)
+        score, _ = path_scores(parent, conf, off)
+        req = np.searchsorted(off, np.arange(C), side="right") - 1
+        glob_parent = np.array([-1 if parent[i] < 0 else off[req[i]] + parent[i] for i in range(C)])
+        kept = set(so.tolist())
+        k = min(budget, C)
+        assert len(kept) == k, t
+        assert all(glob_parent[i] < 0 or glob_parent[i] in kept for i in kept), t
+        best = -1.0
+        for sub in itertools.combinations(range(C), k):
+            ss = set(sub)
+            if all(glob_parent[i] < 0 or glob_parent[i] in ss for i in sub):
+                best = max(best, float(sum(np.float64(score[i]) for i in sub)))
+        assert abs(float(sum(np.float64(score[i]) for i in kept)) - best) < 1e-12, t
+        for r in range(off.size - 1):
+            a, b = oo[r], oo[r + 1]
+            for j in range(a, b):
+                i = so[j]
+                assert req[i] == r and (po[j] == -1) == (parent[i] < 0), t
+                if po[j] >= 0:
+                    assert so[a + po[j]] == glob_parent[i] and po[j] < j - a, t
+        assert np.array_equal(do, draft[so]), t
+
+
+def test_per_request_budget_is_the_shared_rule_on_each_request():
+    rng = np.random.default_rng(32)
+    for t in range(150):
+        parent, conf, off = random_forest(rng, int(rng.integers(1, 6)), 12)
+        k = int(rng.integers(1, 6))
+        draft = np.arange(off[-1], dtype=np.int32)
+        po, do, so, oo = oracle.budget_select(parent, conf, draft, off, k, per_request=True)
+        for r in range(off.size - 1):
+            a, b = off[r], off[r + 1]
+            p1, d1, s1, o1 = oracle.budget_select(parent[a:b], conf[a:b], draft[a:b], np.array([0, b - a]), k)
+            assert po[oo[r]:oo[r + 1]].tolist() == p1.tolist(), t
+            assert (so[oo[r]:oo[r + 1]] - a).tolist() == s1.tolist(), t
+
+
+def test_budget_rejects_invalid_trees():
+    conf = np.ones(4, np.float32)
+    assert oracle.budget_select([0, 0, 1, 2], conf, [0] * 4, [0, 4], 2) is None     # no root
+    assert oracle.budget_select([-1, 1, 0, 0], conf, [0] * 4, [0, 4], 2) is None    # parent not earlier
