@@ -15,8 +15,9 @@ timed on a bounded sample, SM clocks sampled during the timed region, and
 (under "rows") the other hot-path rows timed in the same run: the Q8 pass over
 the same block, the 151936x5120 LM head with fused argmax and tree acceptance,
 the 64-layer stack at M=32 (exact and Q8 passes, Q-vs-exact agreement), the
-two-level verification step (Q pass, splice, exact pass on 32-node trees) and
-the block and head at M=192 with 24 trees.
+two-level verification step (Q pass, splice, exact pass on 32-node trees), the
+block and head at M=192 with 24 trees, and a node budget shared by 24 requests
+against per-request trees of the same size (accepted tokens).
 
 --impl reference times the CPU oracle (the plain C reference of the method)
 on the same workload and metric, a bounded sample of rows per step.
@@ -638,6 +639,61 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
     out["block_head_m192_24trees"] = {"block": roof(ms_b, b_bytes, b_flops), "head_verify": roof(ms_h, h_bytes, h_flops),
                                       "total_us": 1e3 * (ms_b + ms_h), "tensor_peak_tflops": tf,
                                       "tensor_peak_kind": tf_kind}
+
+    # ---- node budget shared across 24 requests vs per-request trees of the same total size.
+    # Synthetic drafter: 32 candidate nodes per request; the children of a node carry
+    # distinct draft tokens whose confidences (each request its own level, halving from the
+    # first child on, summing below 1) are the probabilities that each one is the target's
+    # token; at most one child matches.  The root is the committed token (confidence 1), so
+    # a node's path score is the probability that it is accepted and the shared top-192
+    # maximises the expected accepted length.  The kept nodes go through the head and
+    # acceptance; accepted tokens averaged over seeds.
+    n_req, cand, B = 24, 32, 192
+    C = n_req * cand
+    xc = torch.empty((C, K), dtype=torch.int16, device=dev)
+    synth.activations_dev(1, 2, 14, xc)
+    t_all = torch.cat([w12.w12_lmhead_argmax(xc[i:i + 256], H, ws=ws2) for i in range(0, C, 256)]).cpu().numpy()
+    off_c = torch.from_numpy(np.arange(0, C + 1, cand, dtype=np.int32)).to(dev)
+    acc = {"shared": [], "per_request": []}
+    for trial in range(8):
+        rng = np.random.default_rng(1000 + trial)
+        par_c = np.concatenate([synth.tree(2, 500 + 24 * trial + r, cand, cand) for r in range(n_req)]).astype(np.int32)
+        level = rng.uniform(0.4, 0.95, n_req)
+        conf_c = np.ones(C, np.float32)
+        dr_c = rng.integers(0, V, C).astype(np.int32)
+        for r in range(n_req):
+            r0 = r * cand
+            kids = [[] for _ in range(cand)]
+            for i in range(1, cand):
+                kids[par_c[r0 + i]].append(i)
+            for pn, ch in enumerate(kids):
+                tp = t_all[r0 + pn]
+                u, cum = rng.random(), 0.0
+                for k, i in enumerate(ch):
+                    conf_c[r0 + i] = np.float32(level[r] * 0.5 ** (k + 1) * rng.uniform(0.8, 1.0))
+                    lo = cum
+                    cum += float(conf_c[r0 + i])
+                    if lo <= u < cum:
+                        dr_c[r0 + i] = tp                           # this child is the target's token
+                    elif dr_c[r0 + i] == tp:
+                        dr_c[r0 + i] = (tp + 1 + k) % V             # the others are not
+        p_d, c_d, d_d = (torch.from_numpy(a).to(dev) for a in (par_c, conf_c, dr_c))
+        for name, budget, per in (("shared", B, False), ("per_request", B // n_req, True)):
+            po, do, so, oo, nk = w12.tree_budget_select(p_d, c_d, d_d, off_c, budget, per)
+            xs = w12.gather_rows(xc, so, B)
+            _, pl, _, _ = w12.w12_lmhead_verify(xs, H, po[:B], do[:B], req_offsets=oo, ws=ws2)
+            acc[name].append(int(pl.sum()))
+
+        def budget_step():
+            po, do, so, oo, nk = w12.tree_budget_select(p_d, c_d, d_d, off_c, B, False)
+            xs = w12.gather_rows(xc, so, B)
+            w12.w12_lmhead_verify(xs, H, po[:B], do[:B], req_offsets=oo, ws=ws2)
+
+    ms_bud = timed_ms(torch, budget_step, steps)
+    sh, pr = float(np.mean(acc["shared"])), float(np.mean(acc["per_request"]))
+    out["shared_budget_24x8"] = {"accepted_tokens_shared": sh, "accepted_tokens_per_request": pr,
+                                 "gain": sh / pr - 1.0 if pr else None, "trials": len(acc["shared"]),
+                                 "candidates": C, "budget": B, "select_gather_verify_us": 1e3 * ms_bud}
     del H
     torch.cuda.empty_cache()
     return out

@@ -254,6 +254,36 @@ W12_API int tlv_splice(const int32_t* path_len, const int32_t* path_nodes, const
                        const int32_t* sub_draft, const uint16_t* x_sub, int64_t n, int64_t K, int32_t* parent_out,
                        int32_t* draft_out, int32_t* src_out, uint16_t* x_out, void* stream);
 
+/* Node budget shared across requests.  SpecPilot summary page (onedev.kr/papers/1654),
+ * section "What's different": for batching, one node budget shared by all requests (192
+ * nodes for 24 requests).  The page gives no selection rule; this call uses: request r
+ * owns candidate nodes req_offsets[r]..req_offsets[r+1]-1 (parent relative to the request,
+ * -1 for its root, parent < index); conf[i] in (0, 1] is node i's draft confidence; the
+ * path score is the float product of the confidences from the root (root first, each
+ * multiply rounded); nodes are ranked by (score descending, depth ascending, index
+ * ascending) and the first `budget` are kept over all requests (per_request = 0) or within
+ * each request (per_request != 0).  A child never outranks its parent, so the kept set is
+ * closed under ancestors; with calibrated confidences it maximises the expected number
+ * of accepted nodes.  Kept nodes are renumbered per request in their original order.
+ * Inputs (device): parent[C], conf[C] (fp32), draft[C], req_offsets[n_req+1] with
+ * req_offsets[n_req] = C.  Outputs (device, C entries each suffice): parent_out[k],
+ * draft_out[k], src_out[k] (candidate index of each kept node), offsets_out[n_req+1],
+ * n_kept[1] = k, or -1 for an invalid candidate tree.  One block; asynchronous on
+ * `stream`; allocates nothing.  Errors: W12_ERR_INVALID_ARG (null pointer),
+ * W12_ERR_SHAPE (n_req outside 1..1024, C outside 1..4096, budget < 1). */
+W12_API int tree_budget_select(const int32_t* parent, const float* conf, const int32_t* draft,
+                               const int32_t* req_offsets, int32_t n_req, int32_t C, int32_t budget,
+                               int32_t per_request, int32_t* parent_out, int32_t* draft_out, int32_t* src_out,
+                               int32_t* offsets_out, int32_t* n_kept, void* stream);
+
+/* Row gather for the verify pass of selected or spliced nodes (no counterpart in the
+ * pages: a helper of the two calls above): out[i*K..] = x[src[i]*K..] for i < n, zero
+ * rows where src[i] is outside 0..n_src-1.  x[n_src*K], src[n], out[n*K] are device
+ * buffers owned by the caller; asynchronous on `stream`.  Errors: W12_ERR_INVALID_ARG,
+ * W12_ERR_SHAPE (n < 1, n_src < 1, K outside 1..65535). */
+W12_API int gather_rows(const uint16_t* x, int64_t n_src, const int32_t* src, int64_t n, int64_t K, uint16_t* out,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -69,6 +69,8 @@ SIGNATURES = [
     ("tree_verify_workspace_size", _SZ, [_I64]),
     ("tree_verify", ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
     ("tlv_splice", ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P]),
+    ("tree_budget_select", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    ("gather_rows", ctypes.c_int, [_P, _I64, _P, _I64, _I64, _P, _P]),
 ]
 
 
@@ -339,3 +341,33 @@ def tlv_splice(path_len, path_nodes, bonus, draft_q, x_q, sub_parent, sub_draft,
                             _ptr(x_q), n_q, _ptr(sp), _ptr(sd), _ptr(x_sub), n, K, _ptr(parent), _ptr(draft),
                             _ptr(src), _ptr(x), _stream(stream)))
     return parent, draft, src, x
+
+
+def tree_budget_select(parent, conf, draft, req_offsets, budget: int, per_request: bool = False, stream=None):
+    """Node budget over candidate trees (see include/w12.h): returns (parent, draft, src,
+    offsets, n_kept) as device tensors; the first n_kept entries of parent/draft/src are
+    the kept trees (n_kept = -1 for an invalid candidate tree)."""
+    if conf.dtype != torch.float32 or not conf.is_cuda or not conf.is_contiguous():
+        raise ValueError("conf must be a contiguous float32 CUDA tensor")
+    C = conf.numel()
+    n_req = req_offsets.numel() - 1
+    dev = conf.device
+    po = torch.empty(C, dtype=torch.int32, device=dev)
+    do = torch.empty(C, dtype=torch.int32, device=dev)
+    so = torch.empty(C, dtype=torch.int32, device=dev)
+    oo = torch.empty(n_req + 1, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib().tree_budget_select(_ptr(_i32(parent)), _ptr(conf), _ptr(_i32(draft)), _ptr(_i32(req_offsets)), n_req,
+                                    C, int(budget), int(per_request), _ptr(po), _ptr(do), _ptr(so), _ptr(oo), _ptr(nk),
+                                    _stream(stream)))
+    return po, do, so, oo, nk
+
+
+def gather_rows(x, src, n: int | None = None, stream=None):
+    """out[i] = x[src[i]] (zero rows for indices outside x) for the first n entries of src."""
+    x = _bits16(x)
+    n_src, K = x.shape
+    n = src.numel() if n is None else n
+    out = torch.empty((n, K), dtype=x.dtype, device=x.device)
+    _check(lib().gather_rows(_ptr(x), n_src, _ptr(_i32(src)), n, K, _ptr(out), _stream(stream)))
+    return out

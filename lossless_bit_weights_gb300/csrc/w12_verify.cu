@@ -1,5 +1,5 @@
-// w12_verify.cu - greedy draft-tree acceptance, row argmax and the two-level
-// verification splice.
+// w12_verify.cu - greedy draft-tree acceptance, row argmax, the two-level
+// verification splice and the node budget shared across requests.
 //
 // The SpecPilot summary page (onedev.kr/papers/1654), section "What's
 // different", verifies a draft tree by taking the path whose tokens match the
@@ -172,6 +172,125 @@ __global__ void __launch_bounds__(256) k_tlv_splice(const int32_t* __restrict__ 
   }
 }
 
+// Node budget over several candidate trees, one block.  Scores are the float products of
+// the draft confidences from each root (root first, rounded multiplies), ranked by (score
+// descending, depth ascending, index ascending); the first `budget` are kept over all
+// requests, or within each request when per_request is set.  A child never outranks its
+// parent, so the kept set is closed under ancestors.  Kept nodes are renumbered per
+// request in their original order.  An invalid candidate tree sets *n_kept = -1.
+constexpr int kBudgetMaxNodes = 4096;
+constexpr int kBudgetThreads = 1024;
+
+__global__ void __launch_bounds__(kBudgetThreads) k_budget_select(const int32_t* __restrict__ parent,
+                                                                  const float* __restrict__ conf,
+                                                                  const int32_t* __restrict__ draft,
+                                                                  const int32_t* __restrict__ off, int32_t n_req,
+                                                                  int32_t C, int32_t budget, int32_t per_request,
+                                                                  int32_t* parent_out, int32_t* draft_out,
+                                                                  int32_t* src_out, int32_t* off_out, int32_t* n_kept) {
+  extern __shared__ uint8_t sm[];
+  float* score = reinterpret_cast<float*>(sm);
+  int32_t* depth = reinterpret_cast<int32_t*>(score + C);
+  int32_t* req = depth + C;
+  int32_t* idx = req + C;  // rank < budget ? new index : -1
+  __shared__ int32_t s_bad;
+  __shared__ int32_t s_cnt[kBudgetThreads];
+  if (threadIdx.x == 0) s_bad = (off[0] != 0 || off[n_req] != C) ? 1 : 0;  // requests tile 0..C-1
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) *n_kept = -1;
+    return;
+  }
+  // scores and depths, one request per thread, nodes in order (parents come first)
+  for (int32_t r = threadIdx.x; r < n_req; r += blockDim.x) {
+    const int32_t a = off[r], e = off[r + 1];
+    bool ok = e > a && a >= 0 && e <= C && parent[a] == -1;
+    for (int32_t i = a; ok && i < e; ++i) {
+      req[i] = r;
+      if (i == a) {
+        score[i] = conf[i];
+        depth[i] = 0;
+      } else {
+        const int32_t p = parent[i];
+        ok = p >= 0 && p < i - a;
+        if (ok) {
+          score[i] = __fmul_rn(score[a + p], conf[i]);
+          depth[i] = depth[a + p] + 1;
+        }
+      }
+    }
+    if (!ok) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) *n_kept = -1;
+    return;
+  }
+  // rank = number of nodes before this one in the order (all, or the node's request's)
+  for (int32_t i = threadIdx.x; i < C; i += blockDim.x) {
+    const float si = score[i];
+    const int32_t di = depth[i];
+    int32_t j0 = 0, j1 = C;
+    if (per_request) {
+      j0 = off[req[i]];
+      j1 = off[req[i] + 1];
+    }
+    int32_t rank = 0;
+    for (int32_t j = j0; j < j1; ++j) {
+      const float sj = score[j];
+      rank += (sj > si || (sj == si && (depth[j] < di || (depth[j] == di && j < i)))) ? 1 : 0;
+    }
+    idx[i] = rank < budget ? 0 : -1;
+  }
+  __syncthreads();
+  // per request: new indices in original order, then the request's place in the output
+  for (int32_t r = threadIdx.x; r < n_req; r += blockDim.x) {
+    int32_t n = 0;
+    for (int32_t i = off[r]; i < off[r + 1]; ++i)
+      if (idx[i] >= 0) idx[i] = n++;
+    s_cnt[r % kBudgetThreads] = n;  // n_req <= kBudgetThreads (host check)
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t acc = 0;
+    for (int32_t r = 0; r < n_req; ++r) {
+      const int32_t n = s_cnt[r];
+      s_cnt[r] = acc;
+      off_out[r] = acc;
+      acc += n;
+    }
+    off_out[n_req] = acc;
+    *n_kept = acc;
+  }
+  __syncthreads();
+  for (int32_t r = threadIdx.x; r < n_req; r += blockDim.x) {
+    const int32_t a = off[r], base = s_cnt[r];
+    for (int32_t i = a; i < off[r + 1]; ++i) {
+      if (idx[i] < 0) continue;
+      const int32_t o = base + idx[i];
+      parent_out[o] = i == a ? -1 : idx[a + parent[i]];
+      draft_out[o] = draft[i];
+      src_out[o] = i;
+    }
+  }
+}
+
+// out[i] = x[src[i]] (zero rows where src[i] is outside 0..n_src-1), one block per row.
+__global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ x, int64_t n_src,
+                                                     const int32_t* __restrict__ src, int64_t K,
+                                                     uint16_t* __restrict__ out) {
+  const int64_t i = blockIdx.x;
+  const int32_t s = src[i];
+  const uint16_t* row = (s >= 0 && s < n_src) ? x + (int64_t)s * K : nullptr;
+  uint16_t* o = out + i * K;
+  if ((K % 8) == 0 && (((uintptr_t)x | (uintptr_t)out) & 15u) == 0) {
+    for (int64_t k = threadIdx.x; k < K / 8; k += blockDim.x)
+      reinterpret_cast<uint4*>(o)[k] = row ? reinterpret_cast<const uint4*>(row)[k] : make_uint4(0, 0, 0, 0);
+  } else {
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) o[k] = row ? row[k] : (uint16_t)0;
+  }
+}
+
 }  // namespace
 }  // namespace w12
 
@@ -229,6 +348,41 @@ int tlv_splice(const int32_t* path_len, const int32_t* path_nodes, const int32_t
                                                               sub_draft, x_sub, n, K, parent_out, draft_out, src_out,
                                                               x_out);
   W12_LAUNCH_CHECK("tlv_splice kernel");
+  return W12_OK;
+}
+
+int tree_budget_select(const int32_t* parent, const float* conf, const int32_t* draft, const int32_t* req_offsets,
+                       int32_t n_req, int32_t C, int32_t budget, int32_t per_request, int32_t* parent_out,
+                       int32_t* draft_out, int32_t* src_out, int32_t* offsets_out, int32_t* n_kept, void* stream) {
+  if (!parent || !conf || !draft || !req_offsets || !parent_out || !draft_out || !src_out || !offsets_out || !n_kept)
+    return fail(W12_ERR_INVALID_ARG, "tree_budget_select: null pointer");
+  if (n_req < 1 || n_req > kBudgetThreads || C < 1 || C > kBudgetMaxNodes || budget < 1)
+    return fail(W12_ERR_SHAPE, "tree_budget_select: n_req=%d (1..%d), C=%d (1..%d), budget=%d (>= 1)", n_req,
+                kBudgetThreads, C, kBudgetMaxNodes, budget);
+  const size_t smem = (size_t)C * 16;
+  static int configured[64] = {0};
+  int dev = 0;
+  W12_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= 64 || !configured[dev]) {
+    W12_CUDA_TRY(cudaFuncSetAttribute(k_budget_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kBudgetMaxNodes * 16));
+    if (dev < 64) configured[dev] = 1;
+  }
+  k_budget_select<<<1, kBudgetThreads, smem, (cudaStream_t)stream>>>(parent, conf, draft, req_offsets, n_req, C, budget,
+                                                                    per_request, parent_out, draft_out, src_out,
+                                                                    offsets_out, n_kept);
+  W12_LAUNCH_CHECK("tree_budget_select kernel");
+  return W12_OK;
+}
+
+int gather_rows(const uint16_t* x, int64_t n_src, const int32_t* src, int64_t n, int64_t K, uint16_t* out,
+                void* stream) {
+  if (!x || !src || !out) return fail(W12_ERR_INVALID_ARG, "gather_rows: null pointer");
+  if (n < 1 || n > 0x7FFFFFFF || n_src < 1 || K < 1 || K > kMaxK)
+    return fail(W12_ERR_SHAPE, "gather_rows: n=%lld, n_src=%lld, K=%lld out of range", (long long)n, (long long)n_src,
+                (long long)K);
+  k_gather_rows<<<(unsigned)n, 256, 0, (cudaStream_t)stream>>>(x, n_src, src, K, out);
+  W12_LAUNCH_CHECK("gather_rows kernel");
   return W12_OK;
 }
 
