@@ -50,7 +50,7 @@ struct GemmArgs {
   const uint8_t* base;
   const uint32_t* tile_ptr;
   const uint32_t* esc;
-  int64_t N, KC, T, G;  // T = row blocks * KC units, G = CTAs of the partition
+  int64_t N, KC, T, G;  // T = units of the partition, G = its places (pipelines or CTAs)
   int M;                // tokens of this launch (<= NT)
   int tok0;             // first token of this launch (x tensor-map row)
   float* y;             // EPI_STORE: y[m*ldy + n] (already offset to tok0)
@@ -61,6 +61,9 @@ struct GemmArgs {
   uint32_t* counters;
   uint32_t* error;
   DecodeMul mul;
+  // Last: with the ring at 64..256 tokens decode-issue bound, inserting a field above
+  // measured 6% slower (only the offsets of the members after it changed).
+  int64_t RB;  // row blocks of the matrix
 };
 
 __device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
@@ -94,49 +97,65 @@ __device__ __forceinline__ void tma_x(uint32_t dst, const CUtensorMap* map, int 
 // one deep ring.
 constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 block (16 KB, swizzled)
 
-// NT <= 32: two CTAs per SM; larger NT: one CTA per SM (its x stages are larger).  Two
-// decode groups per CTA in both cases (four groups at NT = 128/192 measured slower overall).
-template <int NT, bool Q8>
+// Launch modes.  A pipeline is a producer warp, two decode groups, an MMA issuer and an x
+// warp, with its own shared memory, barriers and TMEM columns.
+//  kModeOwn  (NT <= 32): two pipelines per CTA, one CTA per SM, each pipeline with its own
+//            unit range (units = row block x 64 columns).  As two CTAs on an SM, the older
+//            one's warps were favoured by the scheduler and it finished its equal share
+//            ~6 us sooner on gate/up (a launch ends with the slower one); as two pipelines
+//            of one CTA they finish together on average.
+//  kModeOne  (NT >= 64): one pipeline per CTA; its x chunks are large.
+//  kModePair (NT >= 64): two pipelines share one range of row-block pairs x 64 columns,
+//            pipeline p on row block 2*pair + p, and one x warp and ring (each stage freed
+//            by both MMA issuers).  Twice the decode warps of kModeOne per SM, at the cost
+//            of stream-K splits over twice as many CTAs per (longer) row: it pays on tall
+//            matrices only.
+enum { kModeOwn = 0, kModeOne = 1, kModePair = 2 };
+
+template <int NT, bool Q8, int MODE>
 struct TcPlan {
-  static constexpr int kBlocksPerSM = NT <= 32 ? 2 : 1;
+  static constexpr bool kWide = MODE == kModePair;
+  static constexpr int kPipes = MODE == kModeOne ? 1 : 2;
+  static constexpr int kParts = MODE == kModeOwn ? 2 : 1;     // places in the partition per CTA
   static constexpr int kGroups = 2;
   static constexpr int kDecoders = kGroups * kBlockTiles;
+  static constexpr int kRoles = kWide ? 2 : 3;                // producer, MMA issuer (, x warp)
   static constexpr int kProducer = kDecoders, kMma = kDecoders + 1, kXWarp = kDecoders + 2;
-  static constexpr int kThreads = (kDecoders + 3) * 32;  // one pipeline
-  // For NT <= 32 two pipelines (each a full producer / decode / MMA set on its own unit
-  // range, shared-memory region and TMEM columns) share one CTA per SM.  As two CTAs on an
-  // SM, the older one's warps were favoured by the scheduler and it finished its equal
-  // share ~6 us sooner on gate/up (a launch ends with the slower one); as two pipelines of
-  // one CTA they finish together on average.
-  static constexpr int kPipes = NT <= 32 ? 2 : 1;
-  static constexpr int kCtaThreads = kPipes * kThreads;
-  static constexpr int kCtasPerSM = NT <= 32 ? 2 / kPipes : 1;
+  static constexpr int kThreads = (kDecoders + kRoles) * 32;  // one pipeline
+  static constexpr int kCtaThreads = kPipes * kThreads + (kWide ? 32 : 0);
+  static constexpr int kCtasPerSM = 1;
+  // Warps are spread over the SM's four sub-partitions (16K registers each); a 21- or
+  // 22-warp CTA puts six on one, so 80 registers a thread is the most that launches.
+  static constexpr int kBoundThreads = kPipes == 1 ? kCtaThreads : kCtaThreads > 704 ? kCtaThreads : 704;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
-#ifndef W12_TC_XSTAGES_BIG
-#define W12_TC_XSTAGES_BIG 2
-#endif
-  static constexpr int kXStages = NT <= 64 ? 4 : W12_TC_XSTAGES_BIG;
+  static constexpr int kXStages = NT <= 64 ? 4 : 2;
+  // shared x region (wide): x stages, then x_full[SX] x_empty[SX]
+  static constexpr int kXRegion = kWide ? (kXStages * kX + 2 * kXStages * 8 + 1023) / 1024 * 1024 : 0;
+  static constexpr int kOffXBar = kXStages * kX;
   static constexpr int kHi = kBlockTiles * kHiTileBytes;
   static constexpr int kLo = Q8 ? 0 : kBlockTiles * kLoTileBytes;
   static constexpr int kOffLo = kHi;
   static constexpr int kOffEsc = kHi + kLo;
   static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
   static constexpr int kRec = kOffHdr + 32;
-  static constexpr int kOffA = kXStages * kX;                 // one A buffer per decode group
+  static constexpr int kOffA = kWide ? 0 : kXStages * kX;     // one A buffer per decode group
   static constexpr int kOffRec = kOffA + kGroups * kABuf;
-  static constexpr int kBudget = (kBlocksPerSM == 2 ? 112 : 224) * 1024;
+  static constexpr int kBudget =
+      kWide ? ((227 * 1024 - kXRegion) / 2) / 1024 * 1024 : (MODE == kModeOne ? 224 : 112) * 1024;
   static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
-  // rec_full[S] rec_empty[S] x_full[SX] x_empty[SX] a_full[G] a_empty[G] epi[G] acc_full acc_empty mma_done
-  static constexpr int kNumBars = 2 * kStages + 2 * kXStages + 3 * kGroups + 3;
+  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[G] a_empty[G] epi[G] acc_full acc_empty mma_done
+  static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 3 * kGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kPipeBytes = (kBytes + 1023) / 1024 * 1024;
-  static constexpr int kCtaBytes = kPipes == 1 ? kBytes : kPipes * kPipeBytes;
+  static constexpr int kCtaBytes = kPipes == 1 ? kBytes : kXRegion + kPipes * kPipeBytes;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
   static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
   static_assert(kCtaBytes <= 227 * 1024, "shared memory plan too large");
+  static_assert((MODE == kModeOwn) == (NT <= 32), "launch mode does not fit the token tile");
+  static_assert(kPipes * kTmemCols <= 512, "tensor memory plan too large");
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -249,40 +268,49 @@ __device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lan
   }
 }
 
-template <int NT, bool Q8, int EPI>
-__global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::kCtasPerSM)
+template <int NT, bool Q8, int MODE, int EPI>
+__global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT, Q8, MODE>::kCtasPerSM)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
-  using P = TcPlan<NT, Q8>;
+  using P = TcPlan<NT, Q8, MODE>;
   constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups;
   constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
   extern __shared__ __align__(1024) uint8_t smem_cta[];
   const int lane = threadIdx.x & 31, gwarp = threadIdx.x >> 5;
   // pipeline and the warp's role index inside it: the decode warps of pipeline p are
   // warps 8p..8p+7 (groups stay aligned to TMEM lane quarters), then each pipeline's
-  // producer, MMA issuer and x loader
-  int pipe = 0, warp = gwarp;
-  if (P::kPipes == 2) {
-    constexpr int nd = P::kDecoders;
-    if (gwarp < 2 * nd) {
-      pipe = gwarp / nd;
-      warp = gwarp % nd;
-    } else {
-      pipe = (gwarp - 2 * nd) / 3;
-      warp = nd + (gwarp - 2 * nd) % 3;
-    }
+  // producer and MMA issuer (and x loader); the shared x loader of a wide CTA comes last
+  constexpr int nd = P::kDecoders, nr = P::kRoles, np = P::kPipes;
+  int pipe = 0, warp = kTcX;
+  if (gwarp < np * nd) {
+    pipe = gwarp / nd;
+    warp = gwarp % nd;
+  } else if (gwarp < np * (nd + nr)) {
+    pipe = (gwarp - np * nd) / nr;
+    warp = nd + (gwarp - np * nd) % nr;
   }
-  const int64_t b = (int64_t)blockIdx.x * P::kPipes + pipe;  // the pipeline's place in the partition
+  // place in the partition: each pipeline has one (kModeOwn), or the CTA has one
+  const int64_t b = (int64_t)blockIdx.x * P::kParts + (P::kParts == 2 ? pipe : 0);
   const bool active = b < a.G;
-  uint8_t* smem = smem_cta + pipe * P::kPipeBytes;
+  uint8_t* smem = smem_cta + P::kXRegion + pipe * P::kPipeBytes;
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t xbase = P::kWide ? smem_u32(smem_cta) : sbase;  // x stage 0
   const uint32_t bar0 = sbase + P::kOffBar;
-  const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S, x_full0 = bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
-  const uint32_t a_full0 = x_empty0 + 8 * SX, a_empty0 = a_full0 + 8 * kTcGroups, epi0 = a_empty0 + 8 * kTcGroups;
+  const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S;
+  const uint32_t x_full0 = P::kWide ? xbase + P::kOffXBar : bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
+  const uint32_t a_full0 = bar0 + 16 * S + (P::kWide ? 0 : 16 * SX), a_empty0 = a_full0 + 8 * kTcGroups;
+  const uint32_t epi0 = a_empty0 + 8 * kTcGroups;
   const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
   // misc: [0] TMEM address, [1+g] stream-K flag of group g, [15] drains finished (four per segment)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
   const int64_t u0 = active ? b * a.T / a.G : 0, u1 = active ? (b + 1) * a.T / a.G : 0;
   const int nun = (int)(u1 - u0);
+  // units this pipeline decodes: with an odd number of row blocks, the last pair of a
+  // wide launch has no second row block
+  int nunp = nun;
+  if (P::kWide && pipe == 1 && (a.RB & 1)) {
+    const int64_t lim = (a.T / a.KC - 1) * a.KC;
+    nunp = (int)(lim < u0 ? 0 : (lim < u1 ? lim - u0 : nun));
+  }
 
   // The next kernel on the stream may start as this one's CTAs retire (programmatic
   // dependent launch): its weight stream does not depend on this kernel's output.
@@ -293,10 +321,11 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
       mbar_init(rec_full0 + 8 * i, 1);
       mbar_init(rec_empty0 + 8 * i, kBlockTiles * 32);
     }
-    for (int i = 0; i < SX; ++i) {
-      mbar_init(x_full0 + 8 * i, 1);
-      mbar_init(x_empty0 + 8 * i, 1);
-    }
+    if (!P::kWide || pipe == 0)
+      for (int i = 0; i < SX; ++i) {
+        mbar_init(x_full0 + 8 * i, 1);
+        mbar_init(x_empty0 + 8 * i, P::kWide ? 2 : 1);  // wide: freed by both MMA issuers
+      }
     for (int i = 0; i < kTcGroups; ++i) {
       mbar_init(a_full0 + 8 * i, kBlockTiles * 32);
       mbar_init(a_empty0 + 8 * i, 1);
@@ -308,7 +337,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
     mbar_init_fence();
   }
   // one warp allocates the TMEM columns of every pipeline (address in pipeline 0's misc[0])
-  uint32_t* misc0 = reinterpret_cast<uint32_t*>(smem_cta + P::kOffMisc);
+  uint32_t* misc0 = reinterpret_cast<uint32_t*>(smem_cta + P::kXRegion + P::kOffMisc);
   if (warp == kTcMma && pipe == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc0)),
                  "n"(P::kPipes * P::kTmemCols)
@@ -318,7 +347,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = misc0[0] + (uint32_t)(pipe * P::kTmemCols);
+  const uint32_t tmem0 = misc0[0];  // kept in a register: the teardown frees exactly this
+  const uint32_t tmem = tmem0 + (uint32_t)(pipe * P::kTmemCols);
   bool bail = false;
 
   if (!active) {
@@ -326,30 +356,45 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
   } else if (warp == kTcProducer) {
     // ---------------------------------------------------------------- weight records
     const uint64_t pol_w = policy_evict_first();
-    // tile_ptr[4u0 + wr .. 4u0 + wr + 95] held across the lanes in three registers; the
-    // third is loaded 8 units before any shuffle reads it.
-    const uint32_t* tpw = a.tile_ptr + 4 * u0;
-    const int64_t TT = 4 * (a.T - u0);  // entries left from tpw on (tile_ptr has 4T+1)
-    int wr = 0;
-    uint32_t w0 = lane <= TT ? __ldg(tpw + lane) : 0u;
-    uint32_t w1 = 32 + lane <= TT ? __ldg(tpw + 32 + lane) : 0u;
-    uint32_t w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
-    const uint8_t* hp = a.hi + u0 * P::kHi;
-    const uint8_t* lp = a.lo + u0 * (kBlockTiles * kLoTileBytes);
+    const int KC = (int)a.KC;
+    const int64_t TR = a.RB * a.KC;  // record units (tile_ptr has 4 TR + 1 entries)
+    int kc = P::kWide ? (int)(u0 % a.KC) : 0;
+    // record unit (row block x 64 columns) of the pipeline's first unit
+    int64_t ru = P::kWide ? (2 * (u0 / a.KC) + pipe) * a.KC + kc : u0;
+    // tile_ptr[4ru + wo ..] in a window of 96 entries held across the lanes in three
+    // registers; the third is loaded 8 units before any shuffle reads it.  A wide
+    // pipeline skips the other pipeline's row block at each pair boundary and reloads.
+    const uint32_t* tpw = nullptr;
+    int64_t TT = 0;  // entries left from tpw on
+    int wo = 0;
+    uint32_t w0 = 0u, w1 = 0u, w2 = 0u;
+    auto window = [&](int64_t r) {
+      tpw = a.tile_ptr + 4 * r;
+      TT = 4 * (TR - r);
+      wo = 0;
+      w0 = lane <= TT ? __ldg(tpw + lane) : 0u;
+      w1 = 32 + lane <= TT ? __ldg(tpw + 32 + lane) : 0u;
+      w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
+    };
+    window(ru);
+    const uint8_t* hp = a.hi + ru * P::kHi;
+    const uint8_t* lp = a.lo + ru * (kBlockTiles * kLoTileBytes);
     int issued = 0, s = 0;
     uint32_t ph = 0;  // parity of the empty phase to wait for, once the ring has wrapped
-    for (int j = 0; j < nun; ++j) {
+    for (int j = 0; j < nunp; ++j) {
       if (j >= S && !warp_wait(rec_empty0 + 8 * s, ph)) {
         bail = true;
         break;
       }
-      if (4 * j - wr >= 32) {
+      if (wo >= 32) {
         w0 = w1;
         w1 = w2;
-        wr += 32;
-        w2 = wr + 64 + lane <= TT ? __ldg(tpw + wr + 64 + lane) : 0u;
+        tpw += 32;
+        TT -= 32;
+        wo -= 32;
+        w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
       }
-      const int src = 4 * j - wr + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4u + i]
+      const int src = wo + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4ru + i]
       const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
       const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
       const uint32_t tpv = src < 32 ? v0 : v1;
@@ -371,10 +416,23 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
       }
       hp += P::kHi;
       lp += kBlockTiles * kLoTileBytes;
+      wo += 4;
       issued = j + 1;
       if (++s == S) {
         s = 0;
         if (j >= S) ph ^= 1u;
+      }
+      if constexpr (P::kWide) {
+        ++ru;
+        if (++kc == KC) {
+          kc = 0;
+          if (j + 1 < nunp) {
+            ru += a.KC;
+            hp += (int64_t)KC * P::kHi;
+            lp += (int64_t)KC * (kBlockTiles * kLoTileBytes);
+            window(ru);
+          }
+        }
       }
     }
     // copies still in flight land before the CTA leaves (they have, unless a wait gave up)
@@ -400,7 +458,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
         }
         const uint32_t xfull = x_full0 + 8 * s;
         mbar_arrive_expect_tx(xfull, P::kX);
-        tma_x(sbase + s * P::kX, &xmap, (int)(kc * kTileK), a.tok0, xfull, pol_x);
+        tma_x(xbase + s * P::kX, &xmap, (int)(kc * kTileK), a.tok0, xfull, pol_x);
         issued = j + 1;
         if (++kc == a.KC) kc = 0;
       }
@@ -415,12 +473,12 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
       // Descriptors are built once: a K step of 16 adds 32 bytes (2 in the 16-byte address
       // field) and an x stage adds kX bytes.  Shared addresses stay below 2^18, so the
       // address field never carries into the neighbouring bits.
-      const uint64_t ad0 = umma_desc(sbase + P::kOffA), xd0 = umma_desc(sbase);
+      const uint64_t ad0 = umma_desc(sbase + P::kOffA), xd0 = umma_desc(xbase);
       const int KC = (int)a.KC;
       int kc = (int)(u0 % a.KC);
       int seg = 0, s = 0, gi = 0;
       uint32_t xph = 0, aph = 0;
-      for (int j = 0; j < nun; ++j) {
+      for (int j = 0; j < nunp; ++j) {
         const bool first = (j == 0) || (kc == 0);
         if (first && j > 0 && !mbar_wait_bounded(acc_empty, (uint32_t)((seg - 1) & 1))) {
           bail = true;
@@ -437,7 +495,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
           umma_bf16(tmem, ad + 2 * ks, xd + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
         umma_commit(a_empty0 + 8 * gi);
         umma_commit(x_empty0 + 8 * s);
-        if (kc + 1 == KC || j + 1 == nun) {
+        if (kc + 1 == KC || j + 1 == nunp) {
           umma_commit(acc_full);
           ++seg;
         }
@@ -451,9 +509,23 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
           aph ^= 1u;
         }
       }
+      // a wide pipeline past its last row block still frees the shared x stages it skips
+      for (int j = nunp; j < nun && !bail; ++j) {
+        if (!mbar_wait_bounded(x_full0 + 8 * s, xph)) {
+          bail = true;
+          break;
+        }
+        mbar_arrive(x_empty0 + 8 * s);
+        if (++s == SX) {
+          s = 0;
+          xph ^= 1u;
+        }
+      }
       // every MMA issued here has finished before TMEM is released
-      umma_commit(mma_done);
-      mbar_wait_bounded(mma_done, 0u);
+      if (nunp > 0) {
+        umma_commit(mma_done);
+        mbar_wait_bounded(mma_done, 0u);
+      }
     }
     __syncwarp();
   } else {
@@ -466,15 +538,16 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
     uint8_t* atp = smem + P::kOffA + gi * kABuf + tl * (kTileRows * 128);
     const uint32_t a_full = a_full0 + 8 * gi, a_empty = a_empty0 + 8 * gi, epi_bar = epi0 + 8 * gi;
     const int KC = (int)a.KC, U0 = (int)u0;
-    const int rb0 = U0 / KC;
+    const int srb0 = U0 / KC;
     int j = gi;
-    int rb = (U0 + j) / KC, kc = (U0 + j) - rb * KC;
+    int srb = (U0 + j) / KC, kc = (U0 + j) - srb * KC;  // partition row (row block or pair) and chunk
     int s = j % S;
     uint32_t ph = (uint32_t)((j / S) & 1);
     int cur_rb = -1, mine = 0;
     uint32_t base2[4];
     uint32_t epi_phase = 0;
-    for (; j < nun; j += kTcGroups) {
+    for (; j < nunp; j += kTcGroups) {
+      const int rb = P::kWide ? 2 * srb + pipe : srb;
       if (rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
         cur_rb = rb;
 #pragma unroll
@@ -483,6 +556,15 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
           const uint32_t bb = n < a.N ? (uint32_t)__ldg(a.base + n) : 1u;
           base2[q] = (bb << 7) | (bb << 23);
         }
+      }
+      // The full barrier's parity wait is exact only while this stage's previous unit
+      // (j - S) has already been consumed.  That holds when it is this group's own unit (S
+      // even) or at least five back (the other group has finished unit j - 5 by now: this
+      // group's previous A buffer was freed by the MMA of unit j - 4, issued after that of
+      // j - 5).  A three-stage ring waits for the release of unit j - 3 first.
+      if (S % 2 == 1 && S < 5 && j >= S && !warp_wait(rec_empty0 + 8 * s, ph ^ 1u)) {
+        bail = true;
+        break;
       }
       if (!warp_wait(rec_full0 + 8 * s, ph)) {
         bail = true;
@@ -536,12 +618,12 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
         mbar_arrive(a_full);
         ++mine;
       }
-      if (kc == KC - 1 || j == nun - 1) {
+      if (kc == KC - 1 || j == nunp - 1) {
         // ---- this unit ends a row block (or the CTA's share of one): the accumulator
         // from TMEM.  seg counts the segments of this CTA before this one.  The drains of
         // the earlier segments (by any group) end first; after them the accumulator
         // barrier is at most one phase from this segment's, so its parity wait is exact.
-        const int seg = rb - rb0;
+        const int seg = srb - srb0;
         if (seg > 0 && !wait_count(misc + 15, 4u * (uint32_t)seg)) {
           bail = true;
           break;
@@ -552,7 +634,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
         }
         tc_fence_after();
         const int64_t rt = (int64_t)rb * kBlockTiles + tl;
-        const bool whole = U0 <= rb * KC && kc == KC - 1;
+        const bool whole = U0 <= srb * KC && kc == KC - 1;
         const uint32_t trow = tmem + ((uint32_t)(tl * 32) << 16);
         if (whole) {
 #pragma unroll 1
@@ -565,11 +647,14 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
           mbar_arrive(acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
         } else {
-          const int64_t cf = cta_of_unit((int64_t)rb * KC, a.G, a.T);
-          const int64_t cl = cta_of_unit((int64_t)(rb + 1) * KC - 1, a.G, a.T);
+          const int64_t cf = cta_of_unit((int64_t)srb * KC, a.G, a.T);
+          const int64_t cl = cta_of_unit((int64_t)(srb + 1) * KC - 1, a.G, a.T);
           const int64_t ncov = cl - cf + 1;
           constexpr int kWarpSlot = NT * 32;  // floats per warp in a slot
-          float4* slot = reinterpret_cast<float4*>(a.slots + ((b + rb) * kBlockTiles + tl) * kWarpSlot);
+          // slot of (part c, row srb): c + srb is unique among the parts covering a row;
+          // a wide launch keeps one per pipeline
+          auto slot_of = [&](int64_t c) { return P::kWide ? 2 * (c + srb) + pipe : c + srb; };
+          float4* slot = reinterpret_cast<float4*>(a.slots + (slot_of(b) * kBlockTiles + tl) * kWarpSlot);
 #pragma unroll 1
           for (int c0 = 0; c0 < NT; c0 += 16) {
             float v[16];
@@ -607,7 +692,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
               for (int i = 0; i < 16; ++i) v[i] = 0.f;
               for (int64_t jj = 0; jj < ncov; ++jj) {
                 const float4* sj =
-                    reinterpret_cast<const float4*>(a.slots + ((cf + rb + jj) * kBlockTiles + tl) * kWarpSlot);
+                    reinterpret_cast<const float4*>(a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   const float4 q4 = __ldcg(sj + (c0 / 4 + i) * 32 + lane);
@@ -631,7 +716,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
       kc += kTcGroups;
       while (kc >= KC) {
         kc -= KC;
-        ++rb;
+        ++srb;
       }
     }
   }
@@ -642,7 +727,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8>::kCtaThreads, TcPlan<NT, Q8>::k
   __syncthreads();
   tc_fence_after();
   if (warp == kTcMma && pipe == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(misc0[0]), "n"(P::kPipes * P::kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem0), "n"(P::kPipes * P::kTmemCols)
                  : "memory");
 }
 
@@ -699,13 +784,23 @@ int device_sms(int* sms) {
   return W12_OK;
 }
 
-// Launch shape for M tokens: tokens per launch (the MMA's N) and CTAs per SM.
+// Launch shape for M tokens on an N x K matrix: tokens per launch (the MMA's N), launch
+// mode and places in the partition per SM.
 struct LaunchShape {
-  int nt, bpsm;
+  int nt, mode, parts;
 };
-LaunchShape launch_shape(int64_t M) {
+LaunchShape launch_shape(int64_t M, int64_t N, int sms) {
   const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 192 ? 192 : 256;
-  return {nt, nt <= 32 ? 2 : 1};
+  if (nt <= 32) return {nt, kModeOwn, 2};
+  // row-block pairs: on matrices with a row block per SM or more, up to 128 tokens
+  const bool pair = nt <= 128 && row_blocks(N) >= sms;
+  return {nt, pair ? kModePair : kModeOne, 1};
+}
+
+// Units of the partition: row block x 64 columns, or row-block pair x 64 columns.
+int64_t partition_units(int64_t N, int64_t K, int mode) {
+  const int64_t RB = row_blocks(N), KC = k_chunks(K);
+  return (mode == kModePair ? (RB + 1) / 2 : RB) * KC;
 }
 
 // CTAs of the stream-K partition for a T-unit problem.
@@ -723,15 +818,17 @@ struct WsLayout {
 
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   const int64_t RB = row_blocks(N), RT = row_tiles(N), KC = k_chunks(K), T = RB * KC;
-  const LaunchShape ls = launch_shape(M);
-  const int64_t G = partition_ctas(T, sms, ls.bpsm);
+  const LaunchShape ls = launch_shape(M, N, sms);
+  const int64_t TP = partition_units(N, K, ls.mode);
+  const int64_t G = partition_ctas(TP, sms, ls.parts);
+  const int64_t n_slots = ls.mode == kModePair ? 2 * ((RB + 1) / 2 + G) : RB + G;
   WsLayout L{};
   L.counters = 0;
   size_t off = align256((size_t)RB * 4);
   L.error = off;
   off += 256;
-  L.slots = off;  // one slot of 128 channels x nt tokens per (CTA, row block) pair
-  off = align256(off + (size_t)(RB + G) * (size_t)(kBlockTiles * kTileRows) * (size_t)ls.nt * 4);
+  L.slots = off;  // one slot of 128 channels x nt tokens per (partition part, row block) pair
+  off = align256(off + (size_t)n_slots * (size_t)(kBlockTiles * kTileRows) * (size_t)ls.nt * 4);
   L.xpad = off;
   off = align256(off + (size_t)M * (size_t)(KC * kTileK) * 2);
   L.pbest = off;
@@ -768,19 +865,19 @@ int make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K, int64_
   return W12_OK;
 }
 
-template <int NT, bool Q8, int EPI>
+template <int NT, bool Q8, int MODE, int EPI>
 int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  using P = TcPlan<NT, Q8>;
+  using P = TcPlan<NT, Q8, MODE>;
   constexpr int smem = P::kCtaBytes;
   static int configured_for_device[64] = {0};
   int dev = 0;
   W12_CUDA_TRY(cudaGetDevice(&dev));
   if (dev >= 64 || !configured_for_device[dev]) {
-    W12_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc<NT, Q8, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    W12_CUDA_TRY(cudaFuncSetAttribute(k_gemm_tc<NT, Q8, MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     if (dev < 64) configured_for_device[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((a.G + P::kPipes - 1) / P::kPipes));
+  cfg.gridDim = dim3((unsigned)((a.G + P::kParts - 1) / P::kParts));
   cfg.blockDim = dim3(P::kCtaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -789,20 +886,22 @@ int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gemm_tc<NT, Q8, EPI>, map, a));
+  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gemm_tc<NT, Q8, MODE, EPI>, map, a));
   W12_LAUNCH_CHECK("w12 gemm kernel (tcgen05)");
   return W12_OK;
 }
 
 template <bool Q8, int EPI>
-int launch_nt(int nt, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  switch (nt) {
-    case 16: return launch_tc<16, Q8, EPI>(map, a, s);
-    case 32: return launch_tc<32, Q8, EPI>(map, a, s);
-    case 64: return launch_tc<64, Q8, EPI>(map, a, s);
-    case 128: return launch_tc<128, Q8, EPI>(map, a, s);
-    case 192: return launch_tc<192, Q8, EPI>(map, a, s);
-    default: return launch_tc<256, Q8, EPI>(map, a, s);
+int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  const bool pair = ls.mode == kModePair;
+  switch (ls.nt) {
+    case 16: return launch_tc<16, Q8, kModeOwn, EPI>(map, a, s);
+    case 32: return launch_tc<32, Q8, kModeOwn, EPI>(map, a, s);
+    case 64: return pair ? launch_tc<64, Q8, kModePair, EPI>(map, a, s) : launch_tc<64, Q8, kModeOne, EPI>(map, a, s);
+    case 128:
+      return pair ? launch_tc<128, Q8, kModePair, EPI>(map, a, s) : launch_tc<128, Q8, kModeOne, EPI>(map, a, s);
+    case 192: return launch_tc<192, Q8, kModeOne, EPI>(map, a, s);
+    default: return launch_tc<256, Q8, kModeOne, EPI>(map, a, s);
   }
 }
 
@@ -847,9 +946,10 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.esc = A->esc;
   a.N = A->N;
   a.KC = KC;
-  a.T = T;
-  const LaunchShape ls = launch_shape(M);
-  a.G = partition_ctas(T, sms, ls.bpsm);
+  a.RB = RB;
+  const LaunchShape ls = launch_shape(M, A->N, sms);
+  a.T = partition_units(A->N, A->K, ls.mode);
+  a.G = partition_ctas(a.T, sms, ls.parts);
   a.ldy = A->N;
   a.slots = reinterpret_cast<float*>(wsb + L.slots);
   a.counters = reinterpret_cast<uint32_t*>(wsb + L.counters);
@@ -865,9 +965,9 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
     a.tok0 = (int)m0;
     if (!argmax) {
       a.y = y + m0 * A->N;
-      st = q8 ? launch_nt<true, EPI_STORE>(ls.nt, map, a, s) : launch_nt<false, EPI_STORE>(ls.nt, map, a, s);
+      st = q8 ? launch_nt<true, EPI_STORE>(ls, map, a, s) : launch_nt<false, EPI_STORE>(ls, map, a, s);
     } else {
-      st = q8 ? launch_nt<true, EPI_ARGMAX>(ls.nt, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls.nt, map, a, s);
+      st = q8 ? launch_nt<true, EPI_ARGMAX>(ls, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls, map, a, s);
     }
     if (st) return st;
   }

@@ -42,7 +42,10 @@ def test_tiny_config(w12, M, q8):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 33, 65), (17, 100, 1000), (32, 64, 128), (33, 70, 190),
-                                   (5, 7, 7), (16, 31, 63), (2, 257, 640), (40, 96, 320), (192, 64, 256)])
+                                   (5, 7, 7), (16, 31, 63), (2, 257, 640), (40, 96, 320), (192, 64, 256),
+                                   # 64..256 tokens: row-block pairs, odd row-block counts, stream-K splits
+                                   (100, 640, 2048), (255, 384, 4160), (129, 1000, 700), (64, 1152, 5120),
+                                   (70, 5248, 1024)])
 @pytest.mark.parametrize("q8", [False, True])
 def test_ragged_shapes(w12, M, N, K, q8):
     W = synth.weights(0, M, N * 7 + K, N, K)
@@ -75,6 +78,28 @@ def test_deterministic_repeats(w12):
     refq = w12.w12_gemm_q8(x, A, ws=ws).clone()
     for _ in range(5):
         assert torch.equal(w12.w12_gemm_q8(x, A, ws=ws), refq)
+
+
+@pytest.mark.parametrize("M", [100, 256])
+def test_deterministic_repeats_wide(w12, M):
+    """Back-to-back launches at 64..256 tokens (row-block pairs, shallow record rings):
+    every launch gives the same bits, and a sample of channels matches the oracle."""
+    N, K = 34816, 5120
+    W = device_weights(0, 0, 2, N, K)
+    A = w12.encode(W)
+    del W
+    x_h = synth.activations(1, 0, 2, M, K)
+    x = to_dev16(x_h)
+    ws = w12.Workspace()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ref = w12.w12_gemm(x, A, ws=ws).clone()
+    for _ in range(40):
+        w12.w12_gemm(x, A, y=y, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    rows = np.sort(np.random.default_rng(M).choice(N, 16, replace=False))
+    y64, B = oracle.gemm(x_h, synth.weight_rows(0, 0, 2, K, rows))
+    assert_gemm_close(ref.cpu().numpy()[:, rows], y64, B, REL)
 
 
 BLOCK = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
