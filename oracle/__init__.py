@@ -40,7 +40,7 @@ def build() -> str:
     if not os.path.exists(SO) or os.path.getmtime(src) > os.path.getmtime(SO):
         tmp = SO + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
-                               "-o", tmp, src])
+                               "-o", tmp, src, "-lm"])
         os.replace(tmp, SO)
     return SO
 
@@ -69,6 +69,10 @@ def _L():
             lib.w12o_tlv_splice.restype = i32
             lib.w12o_budget_select.argtypes = [p, p, p, p, i32, i32, i32, p, p, p, p]
             lib.w12o_budget_select.restype = i32
+            lib.w12o_i8_quantize.argtypes = [p, i64, i64, p, p, p]
+            lib.w12o_i8_quantize.restype = None
+            lib.w12o_cert_argmax.argtypes = [p, i64, i64, p, i64, p, p, p, p, p]
+            lib.w12o_cert_argmax.restype = i64
             _lib = lib
         return _lib
 
@@ -233,3 +237,62 @@ def budget_select(parent, conf, draft, offsets, budget, per_request=False):
     if k < 0:
         return None
     return po[:k].copy(), do[:k].copy(), so[:k].copy(), oo.copy()
+
+
+def i8_quantize(W, threads: int | None = None):
+    """INT8 head of the certified LM-head argmax (same page and section: on H100 the LM
+    head stays in INT8 and a Cauchy-Schwarz bound filters candidates that are then
+    computed exactly).  W holds bf16 bits [N, K].  Returns code [N, K] (sign<<7 | |q|),
+    scale [N] float32 and cbound [N] float32 (the bound's per-channel factor)."""
+    W = _c(W, np.uint16)
+    N, K = W.shape
+    code = np.empty((N, K), np.uint8)
+    scale = np.empty(N, np.float32)
+    cbound = np.empty(N, np.float32)
+    lib = _L()
+    nt = max(1, min(threads or (os.cpu_count() or 1), N))
+    bounds = [(N * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        a, b = bounds[i], bounds[i + 1]
+        if b > a:
+            lib.w12o_i8_quantize(W.ctypes.data + a * K * 2, b - a, K, code.ctypes.data + a * K,
+                                 scale.ctypes.data + a * 4, cbound.ctypes.data + a * 4)
+
+    if nt == 1:
+        run(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(nt)))
+    return code, scale, cbound
+
+
+def cert_argmax(x, W, code, scale, cbound, threads: int | None = None):
+    """Argmax of the exact logits x . W^T for each row of x, through the certified
+    candidates of the INT8 head (code, scale, cbound from i8_quantize).  Returns
+    (idx [M] int32, ncand [M] int32).  Rows of x are split over threads."""
+    x = _c(x, np.uint16)
+    W = _c(W, np.uint16)
+    code = _c(code, np.uint8)
+    scale = _c(scale, np.float32)
+    cbound = _c(cbound, np.float32)
+    M, K = x.shape
+    V = W.shape[0]
+    idx = np.empty(M, np.int32)
+    ncand = np.empty(M, np.int32)
+    lib = _L()
+    nt = max(1, min(threads or (os.cpu_count() or 1), M))
+    bounds = [(M * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        a, b = bounds[i], bounds[i + 1]
+        if b > a:
+            lib.w12o_cert_argmax(x.ctypes.data + a * K * 2, b - a, K, _p(W), V, _p(code), _p(scale), _p(cbound),
+                                 idx.ctypes.data + a * 4, ncand.ctypes.data + a * 4)
+
+    if nt == 1:
+        run(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(nt)))
+    return idx, ncand

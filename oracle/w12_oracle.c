@@ -343,3 +343,109 @@ int32_t w12o_budget_select(const int32_t* parent, const float* conf, const int32
   free(newidx);
   return kept;
 }
+
+/* ---------------------------------------------------------------------------
+ * Certified LM-head argmax (same page and section: on H100 the LM head stays
+ * in INT8 and a Cauchy-Schwarz error bound filters the candidates, which are
+ * then computed exactly; on an RTX PRO 6000 that was slower than a W12 head).
+ * Readings where the sentence is silent:
+ *   - INT8 is symmetric per output channel: s = (float)(max_k |w| / 127)
+ *     (s = 0 for an all-zero row), q = rint(w / s) in [-127, 127] (ties to
+ *     even), stored as the byte sign<<7 | |q|; weights are finite;
+ *   - the approximate logit of channel v is s_v * sum_k x_k q_k.  Its distance
+ *     to the exact logit sum_k x_k w_k is at most
+ *         ||x|| * ( ||w_v - s_v q_v|| + gamma * s_v * ||q_v|| )
+ *     by Cauchy-Schwarz: the first term is the quantization error, the second
+ *     (gamma = (K + 16) * 2^-21) covers a float accumulation of the
+ *     approximate sum, where the products are exact;
+ *     c_v = ||w_v - s_v q_v|| + gamma * s_v * ||q_v|| is kept per channel,
+ *     rounded up to float;
+ *   - candidates are the channels whose approximate logit plus bound reaches
+ *     the largest approximate logit minus bound; their exact logits decide,
+ *     ties to the lowest index, as in w12o_argmax.
+ */
+#include <math.h>
+
+static float round_up_float(double d) {
+  float f = (float)d;
+  if ((double)f < d) f = nextafterf(f, INFINITY);
+  return f;
+}
+
+static double i8_gamma(int64_t K) { return (double)(K + 16) * ldexp(1.0, -21); }
+
+/* code[N*K] (sign<<7 | |q|), scale[N], cbound[N]. */
+void w12o_i8_quantize(const uint16_t* W, int64_t N, int64_t K, uint8_t* code, float* scale, float* cbound) {
+  const double gamma = i8_gamma(K);
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = W + n * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float a = (float)fabs(bf16_value(row[k]));
+      if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    double e2 = 0.0, q2 = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double w = bf16_value(row[k]);
+      double q = 0.0;
+      if (s > 0.0f) {
+        q = rint(w / (double)s);
+        if (q > 127.0) q = 127.0;
+        if (q < -127.0) q = -127.0;
+      }
+      const int iq = (int)q;
+      code[n * K + k] = (uint8_t)((iq < 0 ? 0x80 : 0x00) | (iq < 0 ? -iq : iq));
+      const double d = w - (double)s * q;
+      e2 += d * d;
+      q2 += q * q;
+    }
+    scale[n] = s;
+    cbound[n] = round_up_float(sqrt(e2) + gamma * (double)s * sqrt(q2));
+  }
+}
+
+static double i8_value(uint8_t c) { return (c & 0x80) ? -(double)(c & 0x7F) : (double)(c & 0x7F); }
+
+/* For each of the M rows of x: the argmax over V channels of the exact logits,
+ * found through the certified candidates.  idx[m], ncand[m] (candidates of row
+ * m); returns the total number of candidates. */
+int64_t w12o_cert_argmax(const uint16_t* x, int64_t M, int64_t K, const uint16_t* W, int64_t V, const uint8_t* code,
+                         const float* scale, const float* cbound, int32_t* idx, int32_t* ncand) {
+  int64_t total = 0;
+  double* lo = (double*)malloc(sizeof(double) * (size_t)V);
+  double* hi = (double*)malloc(sizeof(double) * (size_t)V);
+  for (int64_t m = 0; m < M; ++m) {
+    const uint16_t* xr = x + m * K;
+    double nx2 = 0.0;
+    for (int64_t k = 0; k < K; ++k) nx2 += bf16_value(xr[k]) * bf16_value(xr[k]);
+    const double nx = sqrt(nx2);
+    double thr = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+      double a = 0.0;
+      for (int64_t k = 0; k < K; ++k) a += bf16_value(xr[k]) * i8_value(code[v * K + k]);
+      const double approx = (double)scale[v] * a, b = nx * (double)cbound[v];
+      lo[v] = approx - b;
+      hi[v] = approx + b;
+      if (lo[v] > thr) thr = lo[v];
+    }
+    int64_t best = -1, count = 0;
+    double best_val = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+      if (hi[v] < thr) continue;
+      ++count;
+      double L = 0.0;
+      for (int64_t k = 0; k < K; ++k) L += bf16_value(xr[k]) * bf16_value(W[v * K + k]);
+      if (best < 0 || better(L, best_val)) {
+        best = v;
+        best_val = L;
+      }
+    }
+    idx[m] = (int32_t)best;
+    ncand[m] = (int32_t)count;
+    total += count;
+  }
+  free(lo);
+  free(hi);
+  return total;
+}

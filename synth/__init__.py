@@ -65,6 +65,8 @@ def _h():
             lib = ctypes.CDLL(build_host())
             u64, i64, p = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p
             lib.syn_weights_rows.argtypes = [u64, u64, u64, i64, i64, i64, p]
+            lib.syn_weights_rows_ex.argtypes = [u64, u64, u64, i64, i64, i64, ctypes.c_int, p]
+            lib.syn_weights_rows_ex.restype = None
             lib.syn_channel_scales.argtypes = [u64, u64, u64, i64, i64, p]
             lib.syn_activations.argtypes = [u64, u64, u64, i64, i64, p]
             lib.syn_tree.argtypes = [u64, u64, u64, i64, p]
@@ -84,6 +86,8 @@ def _d():
             lib = ctypes.CDLL(build_dev())
             u64, i64, p = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p
             lib.syn_weights_dev.argtypes = [u64, u64, u64, i64, i64, p, p]
+            lib.syn_weights_dev_ex.argtypes = [u64, u64, u64, i64, i64, ctypes.c_int, p, p]
+            lib.syn_weights_dev_ex.restype = ctypes.c_int
             lib.syn_activations_dev.argtypes = [u64, u64, u64, i64, p, p]
             lib.syn_weights_dev.restype = ctypes.c_int
             lib.syn_activations_dev.restype = ctypes.c_int
@@ -101,8 +105,9 @@ def _threads(n_items: int, threads: int | None) -> int:
 
 
 def weights(seed: int, layer: int, tensor: int, N: int, K: int, row0: int = 0, nrows: int | None = None,
-            threads: int | None = None) -> np.ndarray:
-    """bf16 bits (uint16) of rows [row0, row0+nrows) of the N x K weight matrix."""
+            threads: int | None = None, outliers: bool = True) -> np.ndarray:
+    """bf16 bits (uint16) of rows [row0, row0+nrows) of the N x K weight matrix
+    (outliers=False: the head recipe, without the x2^9 outliers)."""
     nrows = N - row0 if nrows is None else nrows
     out = np.empty((nrows, K), dtype=np.uint16)
     if nrows == 0 or K == 0:
@@ -114,7 +119,7 @@ def weights(seed: int, layer: int, tensor: int, N: int, K: int, row0: int = 0, n
     def run(i):
         a, b = bounds[i], bounds[i + 1]
         if b > a:
-            lib.syn_weights_rows(seed, layer, tensor, K, a, b - a, _ptr(out) + (a - row0) * K * 2)
+            lib.syn_weights_rows_ex(seed, layer, tensor, K, a, b - a, int(outliers), _ptr(out) + (a - row0) * K * 2)
 
     if nt == 1:
         run(0)
@@ -124,13 +129,13 @@ def weights(seed: int, layer: int, tensor: int, N: int, K: int, row0: int = 0, n
     return out
 
 
-def weight_rows(seed: int, layer: int, tensor: int, K: int, rows) -> np.ndarray:
+def weight_rows(seed: int, layer: int, tensor: int, K: int, rows, outliers: bool = True) -> np.ndarray:
     """bf16 bits of an arbitrary list of rows (any order) of a weight matrix."""
     rows = np.asarray(rows, dtype=np.int64)
     out = np.empty((len(rows), K), dtype=np.uint16)
     lib = _h()
     for i, r in enumerate(rows):
-        lib.syn_weights_rows(seed, layer, tensor, K, int(r), 1, _ptr(out) + i * K * 2)
+        lib.syn_weights_rows_ex(seed, layer, tensor, K, int(r), 1, int(outliers), _ptr(out) + i * K * 2)
     return out
 
 
@@ -172,12 +177,12 @@ def u64(seed: int, layer: int, tensor: int, count: int, i0: int = 0) -> np.ndarr
 # ----------------------------------------------------------------------------------------------
 # device generation (torch is used only for the buffers and the stream)
 
-def weights_dev(seed: int, layer: int, tensor: int, out, stream=None) -> None:
+def weights_dev(seed: int, layer: int, tensor: int, out, stream=None, outliers: bool = True) -> None:
     """Fill a contiguous torch.uint16/int16 CUDA tensor of shape (N, K) with the weight matrix."""
     import torch
     N, K = out.shape
     s = stream if stream is not None else torch.cuda.current_stream()
-    rc = _d().syn_weights_dev(seed, layer, tensor, N, K, out.data_ptr(), s.cuda_stream)
+    rc = _d().syn_weights_dev_ex(seed, layer, tensor, N, K, int(outliers), out.data_ptr(), s.cuda_stream)
     if rc:
         raise RuntimeError(f"syn_weights_dev failed with CUDA error {rc}")
 
@@ -188,3 +193,19 @@ def activations_dev(seed: int, layer: int, tensor: int, out, stream=None) -> Non
     rc = _d().syn_activations_dev(seed, layer, tensor, out.numel(), out.data_ptr(), s.cuda_stream)
     if rc:
         raise RuntimeError(f"syn_activations_dev failed with CUDA error {rc}")
+
+
+def peaked_activations(seed: int, layer: int, tensor: int, head_rows, beta: float) -> np.ndarray:
+    """bf16 bits of M hidden-state rows that point at given head rows:
+    x_m = bf16(z_m + beta * w_m / ||w_m||), z_m the N(0,1) activation rows (seed, layer,
+    tensor) and w_m = head_rows[m] (bf16 bits, M x K).  A verify pass's final hidden
+    state points at the token it predicts; plain N(0,1) rows leave no top logit."""
+    head_rows = np.asarray(head_rows, np.uint16)
+    M, K = head_rows.shape
+    z = (activations(seed, layer, tensor, M, K).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = (head_rows.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nrm = np.sqrt((w * w).sum(axis=1, keepdims=True))
+    nrm[nrm == 0] = 1.0
+    f = (z + beta * w / nrm).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)

@@ -23,6 +23,8 @@
  *     c < 0.005  -> outlier:  w * 2^9
  *     c < 0.007  -> exact zero with a random sign
  *     c < 0.008  -> bf16 denormal: random sign, mantissa uniform in 1..127
+ * Head recipe (the *_ex calls with outliers = 0): the same without the outliers,
+ * for an INT8 head, whose per-channel scale an outlier would set.
  */
 #ifndef W12_SYNTH_H
 #define W12_SYNTH_H
@@ -155,8 +157,9 @@ SYN_HD float syn_channel_scale(uint64_t key, uint64_t n) {
 #define SYN_T_DENORM 34359738u  /* 0.008 * 2^32 */
 
 /* Weight element number e = n*K + k of a matrix, given its channel scale and
- * the matrix's category and Gaussian sub-stream keys. */
-SYN_HD uint16_t syn_weight(uint64_t key_cat, uint64_t key_gauss, uint64_t e, float scale) {
+ * the matrix's category and Gaussian sub-stream keys.  With outliers == 0 (the
+ * head recipe) the elements drawn as outliers keep their plain Gaussian value. */
+SYN_HD uint16_t syn_weight_ex(uint64_t key_cat, uint64_t key_gauss, uint64_t e, float scale, int outliers) {
   uint64_t c = syn_at(key_cat, e);
   uint32_t cu = (uint32_t)c;
   uint16_t sign = (uint16_t)(((c >> 32) & 1u) << 15);
@@ -167,8 +170,12 @@ SYN_HD uint16_t syn_weight(uint64_t key_cat, uint64_t key_gauss, uint64_t e, flo
   }
   float z = syn_normal(key_gauss, e);
   uint16_t w = syn_bf16_rne(SYN_MUL(z, scale));
-  if (cu < SYN_T_OUTLIER) w = syn_bf16_rne(SYN_MUL(syn_bf16_to_f32(w), 512.0f));
+  if (outliers && cu < SYN_T_OUTLIER) w = syn_bf16_rne(SYN_MUL(syn_bf16_to_f32(w), 512.0f));
   return w;
+}
+
+SYN_HD uint16_t syn_weight(uint64_t key_cat, uint64_t key_gauss, uint64_t e, float scale) {
+  return syn_weight_ex(key_cat, key_gauss, e, scale, 1);
 }
 
 /* Activation element: bf16(N(0,1)). */

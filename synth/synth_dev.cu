@@ -11,12 +11,13 @@
 
 namespace {
 
-__global__ void k_weights(uint64_t key, uint64_t kc, uint64_t kg, int64_t N, int64_t K, uint16_t* out) {
+__global__ void k_weights(uint64_t key, uint64_t kc, uint64_t kg, int64_t N, int64_t K, int outliers,
+                          uint16_t* out) {
   int64_t n = blockIdx.y + (int64_t)blockIdx.z * gridDim.y;
   if (n >= N) return;
   float scale = syn_channel_scale(key, (uint64_t)n);
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < K; k += (int64_t)gridDim.x * blockDim.x)
-    out[n * K + k] = syn_weight(kc, kg, (uint64_t)n * (uint64_t)K + (uint64_t)k, scale);
+    out[n * K + k] = syn_weight_ex(kc, kg, (uint64_t)n * (uint64_t)K + (uint64_t)k, scale, outliers);
 }
 
 __global__ void k_activations(uint64_t key, int64_t count, uint16_t* out) {
@@ -28,8 +29,10 @@ __global__ void k_activations(uint64_t key, int64_t count, uint16_t* out) {
 
 extern "C" {
 
-/* N x K bf16 weight matrix (seed, layer, tensor) into device memory out[N*K]. Returns a cudaError_t. */
-int syn_weights_dev(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t N, int64_t K, void* out, void* stream) {
+/* N x K bf16 weight matrix (seed, layer, tensor) into device memory out[N*K]; outliers = 0 gives
+ * the head recipe. Returns a cudaError_t. */
+int syn_weights_dev_ex(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t N, int64_t K, int outliers, void* out,
+                       void* stream) {
   if (N <= 0 || K <= 0) return 0;
   uint64_t key = syn_key(seed, layer, tensor);
   int64_t gy = N < 65535 ? N : 65535;
@@ -38,8 +41,12 @@ int syn_weights_dev(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t N, i
   if (gx > 64) gx = 64;
   dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)gz);
   k_weights<<<grid, 256, 0, (cudaStream_t)stream>>>(key, syn_substream(key, SYN_S_CAT), syn_substream(key, SYN_S_GAUSS),
-                                                    N, K, (uint16_t*)out);
+                                                    N, K, outliers, (uint16_t*)out);
   return (int)cudaGetLastError();
+}
+
+int syn_weights_dev(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t N, int64_t K, void* out, void* stream) {
+  return syn_weights_dev_ex(seed, layer, tensor, N, K, 1, out, stream);
 }
 
 /* count bf16 N(0,1) activations (seed, layer, tensor) into device memory. */

@@ -10,15 +10,21 @@
 
 /* Rows [row0, row0 + nrows) of the N x K bf16 weight matrix (seed, layer, tensor),
  * row-major into out[nrows * K]. */
-void syn_weights_rows(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t K, int64_t row0,
-                      int64_t nrows, uint16_t* out) {
+void syn_weights_rows_ex(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t K, int64_t row0,
+                         int64_t nrows, int outliers, uint16_t* out) {
   uint64_t key = syn_key(seed, layer, tensor);
   uint64_t kc = syn_substream(key, SYN_S_CAT), kg = syn_substream(key, SYN_S_GAUSS);
   for (int64_t r = 0; r < nrows; ++r) {
     uint64_t n = (uint64_t)(row0 + r);
     float scale = syn_channel_scale(key, n);
-    for (int64_t k = 0; k < K; ++k) out[r * K + k] = syn_weight(kc, kg, n * (uint64_t)K + (uint64_t)k, scale);
+    for (int64_t k = 0; k < K; ++k)
+      out[r * K + k] = syn_weight_ex(kc, kg, n * (uint64_t)K + (uint64_t)k, scale, outliers);
   }
+}
+
+void syn_weights_rows(uint64_t seed, uint64_t layer, uint64_t tensor, int64_t K, int64_t row0,
+                      int64_t nrows, uint16_t* out) {
+  syn_weights_rows_ex(seed, layer, tensor, K, row0, nrows, 1, out);
 }
 
 /* Channel scales s_n for rows [row0, row0 + nrows). */

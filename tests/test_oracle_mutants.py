@@ -4,7 +4,8 @@ The mutant is compiled on the CPU into a temporary library and the pin suite
 (test_oracle_pins.py) runs against it in a child process; the child must
 report a failure.  This shows the pins constrain every step of the oracle:
 window choice, record layout, planes, decode, the 8-bit view, the fp64 GEMM
-and its bound, argmax ties, tree acceptance and the two-level-verification splice.
+and its bound, argmax ties, tree acceptance, the two-level-verification splice, the
+node budget, and the INT8 head's quantizer, bound and certified argmax.
 """
 import os
 import subprocess
@@ -51,6 +52,18 @@ MUTANTS = {
     "budget parents not renumbered": ("parent_out[kept + n] = i == off[r] ? -1 : newidx[off[r] + parent[i]];",
                                       "parent_out[kept + n] = i == off[r] ? -1 : parent[i];"),
     "budget keeps one too many": ("      keep[i] = rank < budget;", "      keep[i] = rank <= budget;"),
+    "i8 scale off 128": ("const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
+    "i8 codes truncate": ("q = rint(w / (double)s);", "q = trunc(w / (double)s);"),
+    "i8 codes round half up": ("q = rint(w / (double)s);", "q = floor(w / (double)s + 0.5);"),
+    "i8 sign bit dropped": ("code[n * K + k] = (uint8_t)((iq < 0 ? 0x80 : 0x00) | (iq < 0 ? -iq : iq));",
+                            "code[n * K + k] = (uint8_t)(iq < 0 ? -iq : iq);"),
+    "i8 bound drops the quantization error": ("cbound[n] = round_up_float(sqrt(e2) + gamma * (double)s * sqrt(q2));",
+                                              "cbound[n] = round_up_float(gamma * (double)s * sqrt(q2));"),
+    "i8 bound halves the quantization error": ("cbound[n] = round_up_float(sqrt(e2) + gamma * (double)s * sqrt(q2));",
+                                               "cbound[n] = round_up_float(0.5 * sqrt(e2) + gamma * (double)s * sqrt(q2));"),
+    "cert threshold uses the upper end": ("      if (lo[v] > thr) thr = lo[v];", "      if (hi[v] > thr) thr = hi[v];"),
+    "cert keeps only the approximate argmax": ("      if (hi[v] < thr) continue;", "      if (hi[v] < thr || lo[v] < thr) continue;"),
+    "cert ties go high": ("      if (best < 0 || better(L, best_val)) {", "      if (best < 0 || !better(best_val, L)) {"),
 }
 
 

@@ -508,3 +508,118 @@ def test_budget_rejects_invalid_trees():
     conf = np.ones(4, np.float32)
     assert oracle.budget_select([0, 0, 1, 2], conf, [0] * 4, [0, 4], 2) is None     # no root
     assert oracle.budget_select([-1, 1, 0, 0], conf, [0] * 4, [0, 4], 2) is None    # parent not earlier
+
+
+# ----------------------------------------------------------------------------- certified INT8 head
+# Same page and section: on H100 the LM head stays in INT8, a Cauchy-Schwarz error
+# bound filters the candidates and those are computed exactly.  The pins: closed forms
+# of the quantizer, the bound containing every exact logit (tight along the error
+# direction), and the certified argmax equal to a brute-force argmax of the exact logits.
+
+def i8_values(code):
+    code = np.asarray(code)
+    return np.where(code & 0x80, -(code & 0x7F).astype(np.int64), (code & 0x7F).astype(np.int64))
+
+
+def test_i8_quantize_unit_scale_is_rint_ties_to_even():
+    """A channel whose largest magnitude is 127 has scale exactly 1, so the codes are
+    the weights rounded half to even, as sign-magnitude bytes."""
+    W = bf16_of_f32([[127.0, 2.5, 3.5, -0.5, -2.5, 0.0, -127.0, 1.5, 0.25, -0.75, 126.5]])
+    code, scale, _ = oracle.i8_quantize(W)
+    assert scale[0] == 1.0
+    assert code[0].tolist() == [127, 2, 4, 0, 0x82, 0, 0xFF, 2, 0, 0x81, 126]
+
+
+def head_like_rows(rng, N, K):
+    """bf16 rows with per-channel scales, a few zeros, denormals and, in some rows, outliers."""
+    s = 0.005 * 10 ** rng.random(N)
+    w = rng.standard_normal((N, K)) * s[:, None]
+    w[rng.random((N, K)) < 0.002] = 0.0
+    out = rng.random((N, K)) < 0.01
+    w[out & (rng.random((N, 1)) < 0.3)] *= 512.0
+    bits = bf16_of_f32(w.astype(np.float32))
+    den = rng.random((N, K)) < 0.001
+    bits[den] = (rng.integers(1, 128, den.sum()) | (rng.integers(0, 2, den.sum()) << 15)).astype(np.uint16)
+    return bits
+
+
+def test_i8_quantize_invariants():
+    rng = np.random.default_rng(21)
+    W = head_like_rows(rng, 60, 200)
+    W[5] = 0                                   # an all-zero channel
+    W[6] = (np.arange(200) % 127 + 1).astype(np.uint16)    # denormals only
+    code, scale, cb = oracle.i8_quantize(W)
+    w = f32_of_bf16(W).astype(np.float64)
+    q = i8_values(code)
+    s = scale.astype(np.float64)
+    amax = np.abs(w).max(axis=1)
+    assert (np.abs(q) <= 127).all() and (np.sign(q) * np.sign(w) >= 0).all()
+    assert ((code & 0x80) == 0)[q == 0].all()           # no negative zero code
+    for n in range(60):
+        if amax[n] == 0:
+            assert s[n] == 0 and (q[n] == 0).all() and cb[n] == 0
+            continue
+        assert abs(q[n, np.argmax(np.abs(w[n]))]) == 127
+        assert abs(s[n] * 127 - amax[n]) <= amax[n] * 2.0 ** -23
+        # every weight within half a step of its code
+        assert (np.abs(w[n] - s[n] * q[n]) <= 0.5 * s[n] * (1 + 1e-12)).all()
+        assert cb[n] >= np.sqrt(((w[n] - s[n] * q[n]) ** 2).sum())
+
+
+def test_i8_bound_contains_exact_logits_and_is_tight_along_the_error():
+    """|exact - approximate| <= ||x|| c for every channel and row; along the error
+    direction the difference reaches ||x|| ||w - s q|| (Cauchy-Schwarz is an equality
+    there), so the quantization term of c cannot be dropped or shrunk."""
+    rng = np.random.default_rng(22)
+    N, K = 48, 320
+    W = head_like_rows(rng, N, K)
+    code, scale, cb = oracle.i8_quantize(W)
+    w = f32_of_bf16(W).astype(np.float64)
+    q = i8_values(code).astype(np.float64)
+    s = scale.astype(np.float64)
+    x = f32_of_bf16(bf16_of_f32(rng.standard_normal((20, K)).astype(np.float32))).astype(np.float64)
+    exact = x @ w.T
+    approx = (x @ q.T) * s[None, :]
+    B = np.sqrt((x * x).sum(1))[:, None] * cb[None, :].astype(np.float64)
+    assert (np.abs(exact - approx) <= B).all()
+    for n in range(N):
+        err = w[n] - s[n] * q[n]
+        if not err.any():
+            continue
+        xe = f32_of_bf16(bf16_of_f32((err / np.abs(err).max()).astype(np.float32))).astype(np.float64)
+        gap = abs(xe @ w[n] - s[n] * (xe @ q[n]))
+        nx = np.sqrt((xe * xe).sum())
+        assert gap <= nx * cb[n]
+        assert gap >= 0.99 * nx * np.sqrt((err * err).sum())
+
+
+@pytest.mark.parametrize("peaked", [False, True])
+def test_cert_argmax_equals_brute_force_argmax(peaked):
+    rng = np.random.default_rng(23 + peaked)
+    V, K, M = 400, 256, 24
+    W = head_like_rows(rng, V, K)
+    w = f32_of_bf16(W).astype(np.float64)
+    z = rng.standard_normal((M, K))
+    if peaked:
+        t = rng.integers(0, V, M)
+        z = z + 6.0 * w[t] / np.linalg.norm(w[t], axis=1, keepdims=True)
+    x = bf16_of_f32(z.astype(np.float32))
+    code, scale, cb = oracle.i8_quantize(W)
+    idx, ncand = oracle.cert_argmax(x, W, code, scale, cb)
+    exact = f32_of_bf16(x).astype(np.float64) @ w.T
+    assert np.array_equal(idx, np.argmax(exact, axis=1))
+    assert (ncand >= 1).all() and (ncand <= V).all()
+    if peaked:
+        assert ncand.mean() < V / 4
+
+
+def test_cert_argmax_all_zero_head_and_single_channel():
+    x = bf16_of_f32(np.ones((2, 8), np.float32))
+    W = np.zeros((3, 8), np.uint16)
+    code, scale, cb = oracle.i8_quantize(W)
+    idx, ncand = oracle.cert_argmax(x, W, code, scale, cb)
+    assert idx.tolist() == [0, 0] and ncand.tolist() == [3, 3]     # a three-way tie: lowest index
+    W1 = bf16_of_f32(np.full((1, 8), -0.5, np.float32))
+    code, scale, cb = oracle.i8_quantize(W1)
+    idx, ncand = oracle.cert_argmax(x, W1, code, scale, cb)
+    assert idx.tolist() == [0, 0] and ncand.tolist() == [1, 1]
