@@ -284,6 +284,52 @@ W12_API int tree_budget_select(const int32_t* parent, const float* conf, const i
 W12_API int gather_rows(const uint16_t* x, int64_t n_src, const int32_t* src, int64_t n, int64_t K, uint16_t* out,
                         void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Certified LM-head argmax over an INT8 head.  The SpecPilot summary page,
+ * section "What's different", keeps the LM head of its H100 build in INT8 and
+ * filters the argmax candidates with a Cauchy-Schwarz error bound, computing
+ * only those exactly (878 -> 482 us there; on an RTX PRO 6000 it was slower
+ * than a W12 head).
+ *
+ * INT8 head of a V x K bf16 head W (finite values), per output channel v:
+ *   scale[v]  = (float)(max_k |w| / 127)   (0 for an all-zero channel)
+ *   q         = rint(w / scale[v]) in [-127, 127], ties to even
+ *   code      = sign<<7 | |q|, one byte per weight, in the W12 hi-plane layout
+ *               (tiles of 32 channels x 64 columns, byte position as for hi;
+ *               w12_i8_code_bytes(V, K) bytes, padding 0)
+ *   cbound[v] = ||w_v - scale[v] q_v|| + (K + 16) 2^-21 scale[v] ||q_v||,
+ *               rounded up: |x.w_v - scale[v] x.q_v| <= ||x|| cbound[v] for
+ *               every x (Cauchy-Schwarz), the second term covering a float
+ *               accumulation of x.q_v.
+ */
+typedef struct w12_i8_head {
+  int64_t V, K;
+  uint8_t* code;   /* 16-byte aligned */
+  float* scale;    /* V */
+  float* cbound;   /* V */
+} w12_i8_head;
+
+W12_API int64_t w12_i8_code_bytes(int64_t V, int64_t K);
+
+/* Fill H (caller-allocated, H->V x H->K) from the bf16 head W[V*K].
+ * Errors: W12_ERR_INVALID_ARG (null or misaligned buffer), W12_ERR_SHAPE. */
+W12_API int w12_i8_encode(const uint16_t* W, const w12_i8_head* H, void* stream);
+
+W12_API size_t w12_cert_head_workspace_size(int64_t M, int64_t V, int64_t K);
+
+/* tok[m] = argmax_v x_m . w_v of the exact logits (lowest index on ties), for
+ * the M rows of x[M*K] bf16.  The approximate logits come from H, the bound
+ * selects candidates (every channel whose approximate logit plus bound reaches
+ * the row's largest approximate logit minus bound, rounded outward), and the
+ * candidates' exact logits are computed in fp64 from `exact`, the W12 form of
+ * the same head.  ncand[m] (may be NULL) receives the candidate count.
+ * Workspace >= w12_cert_head_workspace_size(M, V, K) bytes, first
+ * w12_gemm_counter_bytes(V) bytes zero before first use (as for w12_gemm).
+ * Errors: W12_ERR_INVALID_ARG, W12_ERR_SHAPE (shapes of H and exact differ,
+ * M out of 1..2^20), W12_ERR_BUFFER_TOO_SMALL. */
+W12_API int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, const w12_matrix* exact,
+                                 int32_t* tok, int32_t* ncand, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,11 @@ class w12_matrix(ctypes.Structure):
                 ("n_esc", ctypes.c_int64)]
 
 
+class w12_i8_head(ctypes.Structure):
+    _fields_ = [("V", ctypes.c_int64), ("K", ctypes.c_int64), ("code", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("cbound", ctypes.c_void_p)]
+
+
 # (name, restype, argtypes) of every exported symbol, in include/w12.h order.
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
 _MP = ctypes.POINTER(w12_matrix)
@@ -71,6 +76,10 @@ SIGNATURES = [
     ("tlv_splice", ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P]),
     ("tree_budget_select", ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     ("gather_rows", ctypes.c_int, [_P, _I64, _P, _I64, _I64, _P, _P]),
+    ("w12_i8_code_bytes", _I64, [_I64, _I64]),
+    ("w12_i8_encode", ctypes.c_int, [_P, ctypes.POINTER(w12_i8_head), _P]),
+    ("w12_cert_head_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w12_cert_head_argmax", ctypes.c_int, [_P, _I64, ctypes.POINTER(w12_i8_head), _MP, _P, _P, _P, _SZ, _P]),
 ]
 
 
@@ -371,3 +380,58 @@ def gather_rows(x, src, n: int | None = None, stream=None):
     out = torch.empty((n, K), dtype=x.dtype, device=x.device)
     _check(lib().gather_rows(_ptr(x), n_src, _ptr(_i32(src)), n, K, _ptr(out), _stream(stream)))
     return out
+
+
+# ---------------------------------------------------------------- certified INT8 head
+
+class I8Head:
+    """Device buffers of an INT8 head (include/w12.h, w12_i8_head): codes in the W12
+    hi-plane layout, per-channel scale and bound factor."""
+
+    def __init__(self, V, K, code, scale, cbound):
+        self.V, self.K = int(V), int(K)
+        self.code, self.scale, self.cbound = code, scale, cbound
+        self._desc = w12_i8_head(self.V, self.K, _ptr(code), _ptr(scale), _ptr(cbound))
+
+    def desc(self):
+        return ctypes.byref(self._desc)
+
+    def stream_bytes(self) -> int:
+        """Bytes the approximate-logit GEMM reads: one code byte per (padded) weight and the scales."""
+        return self.code.numel() + 4 * self.V
+
+
+def i8_encode(W: torch.Tensor, stream=None) -> I8Head:
+    """INT8 head of a V x K bf16 head (certified argmax: SpecPilot page, "What's different")."""
+    W = _bits16(W)
+    V, K = W.shape
+    L = lib()
+    dev = W.device
+    code = torch.empty(int(L.w12_i8_code_bytes(V, K)), dtype=torch.uint8, device=dev)
+    scale = torch.empty(V, dtype=torch.float32, device=dev)
+    cbound = torch.empty(V, dtype=torch.float32, device=dev)
+    H = I8Head(V, K, code, scale, cbound)
+    _check(L.w12_i8_encode(_ptr(W), H.desc(), _stream(stream)))
+    return H
+
+
+def cert_head_workspace_size(M: int, V: int, K: int) -> int:
+    return int(lib().w12_cert_head_workspace_size(M, V, K))
+
+
+def w12_cert_head_argmax(x: torch.Tensor, H: I8Head, exact: W12Matrix, tok: torch.Tensor | None = None,
+                         ncand: torch.Tensor | None = None, ws: Workspace | None = None, stream=None):
+    """Exact-logit argmax of x . W^T through the INT8 head's certified candidates; the
+    exact logits of the candidates come from `exact` (the W12 form of the same head).
+    Returns (tok [M] int32, ncand [M] int32)."""
+    x = _bits16(x)
+    M = x.shape[0]
+    if x.shape[1] != H.K:
+        raise ValueError(f"x has {x.shape[1]} columns, head has K={H.K}")
+    tok = torch.empty(M, dtype=torch.int32, device=x.device) if tok is None else _i32(tok)
+    ncand = torch.empty(M, dtype=torch.int32, device=x.device) if ncand is None else _i32(ncand)
+    ws = ws or Workspace(x.device)
+    buf = ws.get(cert_head_workspace_size(M, H.V, H.K))
+    _check(lib().w12_cert_head_argmax(_ptr(x), M, H.desc(), exact.desc(), _ptr(tok), _ptr(ncand), _ptr(buf),
+                                      buf.numel(), _stream(stream)))
+    return tok, ncand

@@ -42,7 +42,9 @@ namespace {
 constexpr int kEscRun = 128;  // escape entries a record stage holds
 constexpr int kMinIters = 4;  // fewest units per CTA
 
-enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1 };
+// EPI_I8: the weights are INT8 codes (sign<<7 | |q|, in the hi-plane layout; no lo plane,
+// window bases or escapes) and the output is scale[n] * acc.
+enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_I8 = 2 };
 
 struct GemmArgs {
   const uint8_t* hi;
@@ -64,6 +66,7 @@ struct GemmArgs {
   // Last: with the ring at 64..256 tokens decode-issue bound, inserting a field above
   // measured 6% slower (only the offsets of the members after it changed).
   int64_t RB;  // row blocks of the matrix
+  const float* scale;  // EPI_I8: per-channel scale
 };
 
 __device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
@@ -158,6 +161,35 @@ struct TcPlan {
   static_assert(kPipes * kTmemCols <= 512, "tensor memory plan too large");
 };
 
+// 16 INT8 codes (sign<<7 | |q|, in the hi-plane byte order) -> 8 exact bf16 pairs.  A byte
+// permute places each code in the low byte of a 16-bit lane and its sign across the high
+// byte; masking in 0x4300 gives the bf16 +-(128 + |q|), and subtracting +-128 (same sign)
+// leaves +-|q| exactly.
+__device__ __forceinline__ uint32_t i8_pair(uint32_t t) {
+  const uint32_t v = (t & 0x807F807Fu) | 0x43004300u, w = (t & 0x80008000u) | 0x43004300u;
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(w));
+  return d;
+}
+
+// prmt in its default mode: selector nibble bits 2..0 pick a byte, bit 3 fills the result
+// byte with the picked byte's sign bit.
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ void decode16_i8(uint4 h, uint32_t out[8]) {
+  const uint32_t H[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    // pair 2s = bytes 0 and 2 (columns 4s, 4s+1); pair 2s+1 = bytes 1 and 3
+    out[2 * s] = i8_pair(prmt_sign(H[s], 0xA280u));
+    out[2 * s + 1] = i8_pair(prmt_sign(H[s], 0xB391u));
+  }
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
@@ -249,6 +281,13 @@ __device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lan
       const int tok = c0 + i;
       if (tok < a.M && n < a.N) a.y[(int64_t)tok * a.ldy + n] = v[i];
     }
+  } else if (EPI == EPI_I8) {
+    const float sc = n < a.N ? a.scale[n] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = c0 + i;
+      if (tok < a.M && n < a.N) a.y[(int64_t)tok * a.ldy + n] = v[i] * sc;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -272,6 +311,8 @@ template <int NT, bool Q8, int MODE, int EPI>
 __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT, Q8, MODE>::kCtasPerSM)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
   using P = TcPlan<NT, Q8, MODE>;
+  constexpr bool I8 = EPI == EPI_I8;  // INT8 codes: no window bases, escapes or lo plane
+  static_assert(!I8 || Q8, "INT8 codes use the 8-bit record plan");
   constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups;
   constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
   extern __shared__ __align__(1024) uint8_t smem_cta[];
@@ -376,7 +417,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       w1 = 32 + lane <= TT ? __ldg(tpw + 32 + lane) : 0u;
       w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
     };
-    window(ru);
+    if constexpr (!I8) window(ru);
     const uint8_t* hp = a.hi + ru * P::kHi;
     const uint8_t* lp = a.lo + ru * (kBlockTiles * kLoTileBytes);
     int issued = 0, s = 0;
@@ -386,26 +427,29 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         bail = true;
         break;
       }
-      if (wo >= 32) {
-        w0 = w1;
-        w1 = w2;
-        tpw += 32;
-        TT -= 32;
-        wo -= 32;
-        w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
+      uint32_t esc_bytes = 0u, e0 = 0u;
+      if constexpr (!I8) {
+        if (wo >= 32) {
+          w0 = w1;
+          w1 = w2;
+          tpw += 32;
+          TT -= 32;
+          wo -= 32;
+          w2 = 64 + lane <= TT ? __ldg(tpw + 64 + lane) : 0u;
+        }
+        const int src = wo + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4ru + i]
+        const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
+        const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
+        const uint32_t tpv = src < 32 ? v0 : v1;
+        const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
+        e0 = t_first & ~3u;
+        uint32_t e1 = (t_last + 3u) & ~3u;
+        if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
+        esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
+        uint8_t* rec = smem + P::kOffRec + s * P::kRec;
+        if (lane < 6) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = lane < 5 ? tpv : e0;
+        __syncwarp();
       }
-      const int src = wo + (lane < 5 ? lane : 0);  // lane i < 5 gets tile_ptr[4ru + i]
-      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
-      const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
-      const uint32_t tpv = src < 32 ? v0 : v1;
-      const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
-      const uint32_t e0 = t_first & ~3u;
-      uint32_t e1 = (t_last + 3u) & ~3u;
-      if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
-      const uint32_t esc_bytes = t_last > t_first ? (e1 - e0) * 4u : 0u;
-      uint8_t* rec = smem + P::kOffRec + s * P::kRec;
-      if (lane < 6) reinterpret_cast<uint32_t*>(rec + P::kOffHdr)[lane] = lane < 5 ? tpv : e0;
-      __syncwarp();
       if (lane == 0) {
         const uint32_t full = rec_full0 + 8 * s;
         const uint32_t recs = sbase + P::kOffRec + s * P::kRec;
@@ -430,7 +474,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
             ru += a.KC;
             hp += (int64_t)KC * P::kHi;
             lp += (int64_t)KC * (kBlockTiles * kLoTileBytes);
-            window(ru);
+            if constexpr (!I8) window(ru);
           }
         }
       }
@@ -548,7 +592,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     uint32_t epi_phase = 0;
     for (; j < nunp; j += kTcGroups) {
       const int rb = P::kWide ? 2 * srb + pipe : srb;
-      if (rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
+      if (!I8 && rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
         cur_rb = rb;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -582,7 +626,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         }
         // this row tile's escapes: entry ta + lane into a register (the rare tail past 32 stays in memory)
         const uint32_t* hdr = reinterpret_cast<const uint32_t*>(rec + P::kOffHdr);
-        const uint32_t ta = hdr[tl], tb = hdr[tl + 1], e0 = hdr[5];
+        const uint32_t ta = I8 ? 0u : hdr[tl], tb = I8 ? 0u : hdr[tl + 1], e0 = I8 ? 0u : hdr[5];
         const uint32_t cnt = tb - ta;
         uint32_t ent = 0u;
         if ((uint32_t)lane < cnt) {
@@ -601,7 +645,10 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t pr[8];
-          decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr);
+          if constexpr (I8)
+            decode16_i8(hq[q], pr);
+          else
+            decode16<Q8>(hq[q], lq[q], base2[q], a.mul, pr);
           uint8_t* row = atp + (8 * q + g) * 128;
           *reinterpret_cast<uint4*>(row + (((2 * t) ^ g) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
           *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
@@ -906,8 +953,9 @@ int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, 
 }
 
 int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_t* tok, bool q8, bool argmax,
-             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn) {
-  int st = check_matrix(A, !q8, fn);
+             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn, const float* i8_scale = nullptr) {
+  // i8_scale: A->hi holds INT8 codes (the caller has checked A's shape and pointers)
+  int st = i8_scale ? W12_OK : check_matrix(A, !q8, fn);
   if (st) return st;
   if (!x || (!argmax && !y) || (argmax && !tok)) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
@@ -957,13 +1005,17 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.pbest = reinterpret_cast<unsigned long long*>(wsb + L.pbest);
   a.ldp = M;
   a.mul = W12_DECODE_MUL;
+  a.scale = i8_scale;
   CUtensorMap map;
   if ((st = make_x_map(&map, xs, M, A->K, ldx, ls.nt))) return st;
   for (int64_t m0 = 0; m0 < M; m0 += ls.nt) {
     const int Mg = (int)std::min<int64_t>(ls.nt, M - m0);
     a.M = Mg;
     a.tok0 = (int)m0;
-    if (!argmax) {
+    if (i8_scale) {
+      a.y = y + m0 * A->N;
+      st = launch_nt<true, EPI_I8>(ls, map, a, s);
+    } else if (!argmax) {
       a.y = y + m0 * A->N;
       st = q8 ? launch_nt<true, EPI_STORE>(ls, map, a, s) : launch_nt<false, EPI_STORE>(ls, map, a, s);
     } else {
@@ -979,6 +1031,17 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
 }
 
 }  // namespace
+
+// used by w12_cert.cu: y[M x V] = scale[v] * (x . codes^T) for an INT8 head whose code plane
+// (hi-plane layout) is codes; ws as for w12_gemm.
+int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float* scale, int64_t V, int64_t K,
+                 float* y, void* ws, size_t ws_bytes, cudaStream_t s, const char* fn) {
+  w12_matrix A{};
+  A.N = V;
+  A.K = K;
+  A.hi = const_cast<uint8_t*>(codes);
+  return run_gemm(x, M, &A, y, nullptr, true, false, ws, ws_bytes, s, fn, scale);
+}
 
 // used by w12_verify.cu
 int lmhead_argmax_impl(const uint16_t* x, int64_t M, const w12_matrix* head, int32_t* tok, bool q8, void* ws,
