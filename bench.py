@@ -58,7 +58,7 @@ def parse_args():
     p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack rows (32 GB of W12)")
-    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead"], default=None,
+    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead", "cert"], default=None,
                    help="profiling case: repeat one matrix's GEMM (or the LM head) and print its time")
     p.add_argument("--q8", action="store_true", help="with --only: the 8-bit-view GEMM")
     return p.parse_args()
@@ -66,6 +66,7 @@ def parse_args():
 
 def run_only(args):
     """One matrix, repeated: the small case ncu captures (one kernel, few launches)."""
+    import numpy as np
     import torch
 
     import lossless_bit_weights_gb300 as w12
@@ -73,6 +74,30 @@ def run_only(args):
 
     torch.cuda.set_device(0)
     M = args.M
+    if args.only == "cert":
+        # certified INT8 head on the head recipe, M rows pointing at random tokens
+        V, K = LMHEAD
+        W = torch.empty((V, K), dtype=torch.int16, device="cuda")
+        synth.weights_dev(0, 0, 9, W, outliers=False)
+        H, A = w12.i8_encode(W), w12.encode(W)
+        del W
+        torch.cuda.empty_cache()
+        tgt = np.random.default_rng(16).integers(0, V, M)
+        x = torch.from_numpy(synth.peaked_activations(1, 0, 101, synth.weight_rows(0, 0, 9, K, tgt, outliers=False),
+                                                      8.0).view(np.int16)).cuda()
+        ws = w12.Workspace()
+        for _ in range(args.warmup):
+            tok, nc = w12.w12_cert_head_argmax(x, H, A, ws=ws)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            tok, nc = w12.w12_cert_head_argmax(x, H, A, ws=ws)
+        b.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"only": "cert", "M": M, "V": V, "K": K, "us": 1e3 * a.elapsed_time(b) / args.steps,
+                          "ncand": nc.cpu().tolist()}), flush=True)
+        return
     if args.only == "lmhead":
         tensor, (N, K) = 9, LMHEAD
     else:
@@ -695,6 +720,38 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
                                  "gain": sh / pr - 1.0 if pr else None, "trials": len(acc["shared"]),
                                  "candidates": C, "budget": B, "select_gather_verify_us": 1e3 * ms_bud}
     del H
+    torch.cuda.empty_cache()
+
+    # ---- certified INT8 head against the W12 head on the same weights: the head recipe
+    # (no x2^9 outliers, which would set every channel's INT8 scale) and 16 rows pointing
+    # at random tokens (a verify pass's final hidden state points at the token it
+    # predicts); then 16 plain N(0,1) rows, where no logit stands out.
+    W = torch.empty((V, K), dtype=torch.int16, device=dev)
+    synth.weights_dev(0, 0, 9, W, outliers=False)
+    Hc, Ac = w12.i8_encode(W), w12.encode(W)
+    del W
+    torch.cuda.empty_cache()
+    tgt = np.random.default_rng(16).integers(0, V, M)
+    rows = synth.weight_rows(0, 0, 9, K, tgt, outliers=False)
+    cert = {"rows": M, "beta": 8.0, "weights": "head recipe (no x2^9 outliers)"}
+    xn = torch.empty((M, K), dtype=torch.int16, device=dev)
+    synth.activations_dev(1, 0, 103, xn)
+    xp = torch.from_numpy(synth.peaked_activations(1, 0, 101, rows, 8.0).view(np.int16)).to(dev)
+    for name, xr in (("peaked", xp), ("isotropic", xn)):
+        tok_c, nc = w12.w12_cert_head_argmax(xr, Hc, Ac, ws=ws2)
+        tok_w = w12.w12_lmhead_argmax(xr, Ac, ws=ws2)
+        ms_w = timed_ms(torch, lambda: w12.w12_lmhead_argmax(xr, Ac, ws=ws2), steps)
+        ms_c = timed_ms(torch, lambda: w12.w12_cert_head_argmax(xr, Hc, Ac, ws=ws2), steps)
+        nc = nc.cpu().numpy()
+        cert[name] = {"w12_head_us": 1e3 * ms_w, "cert_int8_head_us": 1e3 * ms_c, "speedup": ms_w / ms_c,
+                      "candidates_mean": float(nc.mean()), "candidates_max": int(nc.max()),
+                      "same_tokens_as_w12_head": bool(torch.equal(tok_c, tok_w)),
+                      "int8_stream_GBps": (Hc.stream_bytes() + 2 * M * K) / (ms_c * 1e-3) / 1e9,
+                      "w12_stream_GBps": (Ac.stream_bytes() + 2 * M * K) / (ms_w * 1e-3) / 1e9}
+        if name == "peaked":
+            cert[name]["rows_on_target"] = int((tok_c.cpu().numpy() == tgt).sum())
+    out["cert_head_m16"] = cert
+    del Hc, Ac
     torch.cuda.empty_cache()
     return out
 

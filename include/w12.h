@@ -321,8 +321,8 @@ W12_API size_t w12_cert_head_workspace_size(int64_t M, int64_t V, int64_t K);
  * the M rows of x[M*K] bf16.  The approximate logits come from H, the bound
  * selects candidates (every channel whose approximate logit plus bound reaches
  * the row's largest approximate logit minus bound, rounded outward), and the
- * candidates' exact logits are computed in fp64 from `exact`, the W12 form of
- * the same head.  ncand[m] (may be NULL) receives the candidate count.
+ * candidates' logits are recomputed from `exact`, the W12 form of the same head
+ * (exact bf16 products, a float-pair sum whose error is near 2^-48 sum|x*w|).  ncand[m] (may be NULL) receives the candidate count.
  * Workspace >= w12_cert_head_workspace_size(M, V, K) bytes, first
  * w12_gemm_counter_bytes(V) bytes zero before first use (as for w12_gemm).
  * Errors: W12_ERR_INVALID_ARG, W12_ERR_SHAPE (shapes of H and exact differ,

@@ -13,9 +13,9 @@
 //   - candidates are the channels whose approximate logit plus bound reaches
 //     the row's largest approximate logit minus bound; every bound and
 //     comparison is rounded outward, so the exact argmax is always among them;
-//   - each candidate's exact logit is recomputed in fp64 from the lossless W12
-//     form of the same head (decode of one channel), and the largest wins,
-//     ties to the lowest index.
+//   - each candidate's exact logit is recomputed from the lossless W12 form of
+//     the same head (decode of one channel; exact products, a float-pair sum),
+//     and the largest wins, ties to the lowest index.
 #include <cstdint>
 
 #include "w12_internal.cuh"
@@ -27,8 +27,9 @@ int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float
 
 namespace {
 
-constexpr int kExactBlocks = 16;  // blocks per row of the exact recompute
-constexpr int kExactWarps = 8;
+constexpr int kExactBlocks = 256;  // blocks per row of the exact recompute
+constexpr int kThrBlocks = 64;     // blocks per row of the threshold
+constexpr int kExactWarps = 10;    // 10 x 8 chunks: K = 5120 in one round
 
 inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
@@ -104,38 +105,56 @@ __global__ void __launch_bounds__(256) k_i8_encode(const uint16_t* __restrict__ 
   }
 }
 
-// nx[m] >= ||x_m||, rounded up to float.
+// nx[m] >= ||x_m||: every square and every addition rounds
+// up, so the sum (and its square root, rounded up) bound the norm from above.
 __global__ void __launch_bounds__(256) k_rownorm(const uint16_t* __restrict__ x, int64_t K, float* __restrict__ nx) {
-  __shared__ double shd[32];
+  __shared__ float shf[32];
   const uint16_t* xr = x + (int64_t)blockIdx.x * K;
-  double a = 0.0;
+  float a = 0.f;
   for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
-    const double f = (double)bf16f(xr[k]);
-    a += f * f;
+    const float f = bf16f(xr[k]);
+    a = __fadd_ru(a, __fmul_ru(f, f));
   }
-  a = block_sum(a, shd);
-  if (threadIdx.x == 0) nx[blockIdx.x] = __double2float_ru(__dsqrt_ru(a));
+  for (int o = 16; o > 0; o >>= 1) a = __fadd_ru(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((threadIdx.x & 31) == 0) shf[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = __fadd_ru(t, shf[w]);
+    nx[blockIdx.x] = __fsqrt_ru(t);
+  }
 }
 
-// thr[m] = max_v (approx[m,v] - bound[m,v]), every step rounded down.
+// Order-preserving map of floats to unsigned keys (larger float, larger key; key 0 is
+// below every float), so that a maximum can be taken with atomicMax in any order.
+__device__ __forceinline__ uint32_t fkey(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// thr[m] = max_v (approx[m,v] - bound[m,v]), every step rounded down; thr_key zero beforehand.
 __global__ void __launch_bounds__(1024) k_cert_thr(const float* __restrict__ lh, int64_t V, const float* __restrict__ nx,
-                                                   const float* __restrict__ cb, float* __restrict__ thr) {
+                                                   const float* __restrict__ cb, uint32_t* __restrict__ thr_key) {
   __shared__ float shf[32];
-  const int64_t m = blockIdx.x;
+  const int64_t m = blockIdx.y;
   const float n = nx[m];
   float t = -INFINITY;
-  for (int64_t v = threadIdx.x; v < V; v += blockDim.x) t = fmaxf(t, __fsub_rd(lh[m * V + v], __fmul_ru(n, cb[v])));
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < V; v += (int64_t)gridDim.x * blockDim.x)
+    t = fmaxf(t, __fsub_rd(lh[m * V + v], __fmul_ru(n, cb[v])));
   t = block_max(t, shf);
-  if (threadIdx.x == 0) thr[m] = t;
+  if (threadIdx.x == 0) atomicMax(thr_key + m, fkey(t));
 }
 
 // Candidates: approx + bound (rounded up) >= thr.
 __global__ void __launch_bounds__(1024) k_cert_cand(const float* __restrict__ lh, int64_t V, const float* __restrict__ nx,
-                                                    const float* __restrict__ cb, const float* __restrict__ thr,
+                                                    const float* __restrict__ cb, const uint32_t* __restrict__ thr_key,
                                                     int32_t* __restrict__ count, int32_t* __restrict__ cand) {
   const int64_t m = blockIdx.y, v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= V) return;
-  if (__fadd_ru(lh[m * V + v], __fmul_ru(nx[m], cb[v])) >= thr[m]) {
+  if (__fadd_ru(lh[m * V + v], __fmul_ru(nx[m], cb[v])) >= fkey_inv(thr_key[m])) {
     const int pos = atomicAdd(count + m, 1);
     cand[m * V + pos] = (int32_t)v;
   }
@@ -146,41 +165,57 @@ struct Best {
   int32_t idx;  // -1: none
 };
 
+// Error-free float addition (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// (hi, lo) += p with the rounding error of the high part carried in lo.
+__device__ __forceinline__ void acc2(float& hi, float& lo, float p) {
+  float e;
+  two_sum(hi, p, hi, e);
+  lo = __fadd_rn(lo, e);
+}
+
 __device__ __forceinline__ bool beats(double a, int32_t ia, double b, int32_t ib) {
   if (ia < 0) return false;
   if (ib < 0) return true;
   return a > b || (a == b && ia < ib);
 }
 
-// Exact logits of the candidates in fp64 from the W12 head: warp w of block b takes
-// candidates b*8 + w, stepping by 16 blocks x 8 warps.  Lane 4*c8 + t decodes the 16
-// columns 16t.. of chunk kc0 + c8 (the same decode as the GEMM), patches the channel's
-// escapes in them and multiplies by x.
+// Exact logits of the candidates from the W12 head.  Block b of row m takes candidates
+// b, b + gridDim.x, ...; its 10 warps split the candidate's column chunks: lane 4*c8 + t
+// of warp w decodes the 16 columns 16t.. of chunks w*8 + c8 + 80i (the same decode as
+// the GEMM) and patches the channel's escapes in them.  A product of two bf16 values is
+// exact in float; the sum is a float pair (TwoSum), whose error is near 2^-48 of
+// sum|x*w|, far inside the argmax's tie tolerance and on the full-rate float pipe
+// (float64 runs at a small fraction of it on this GPU).
 __global__ void __launch_bounds__(kExactWarps * 32)
     k_cert_exact(const uint16_t* __restrict__ x, int64_t K, int64_t KC, const uint8_t* __restrict__ hi,
                  const uint8_t* __restrict__ lo, const uint8_t* __restrict__ base, const uint32_t* __restrict__ tile_ptr,
                  const uint32_t* __restrict__ esc, const int32_t* __restrict__ count, const int32_t* __restrict__ cand,
                  int64_t V, DecodeMul mul, Best* __restrict__ part) {
-  __shared__ Best sh[kExactWarps];
+  __shared__ float shh[kExactWarps], shl[kExactWarps];
   const int64_t m = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c8 = lane >> 2, t = lane & 3;
   const int n_c = count[m];
   const uint16_t* xr = x + m * K;
   Best best{0.0, -1};
-  for (int i = blockIdx.x * kExactWarps + warp; i < n_c; i += kExactBlocks * kExactWarps) {
+  for (int i = blockIdx.x; i < n_c; i += gridDim.x) {
     const int64_t v = cand[m * V + i];
     const int64_t rt = v / kTileRows;
     const int r = (int)(v % kTileRows), q = r >> 3, g = r & 7;
     const uint32_t bb = base[v];
     const uint32_t base2 = (bb << 7) | (bb << 23);
-    double acc = 0.0;
-    for (int64_t kc0 = 0; kc0 < KC; kc0 += 8) {
-      const int64_t kc = kc0 + c8;
-      if (kc >= KC) continue;
+    float ah = 0.f, al = 0.f;
+    for (int64_t kc = warp * 8 + c8; kc < KC; kc += kExactWarps * 8) {
       const int64_t tile = tile_index(rt, kc, KC);
       const uint4 hq = *reinterpret_cast<const uint4*>(hi + tile * kHiTileBytes + q * 512 + (4 * g + t) * 16);
       const uint2 lq = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
+      const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
       uint32_t pr[8];
       decode16<false>(hq, lq, base2, mul, pr);
       uint16_t w[16];
@@ -189,44 +224,75 @@ __global__ void __launch_bounds__(kExactWarps * 32)
         w[2 * p] = (uint16_t)(pr[p] & 0xFFFFu);
         w[2 * p + 1] = (uint16_t)(pr[p] >> 16);
       }
-      for (uint32_t e = tile_ptr[tile]; e < tile_ptr[tile + 1]; ++e) {
-        const uint32_t ent = esc[e];
-        const int c = esc_col(ent);
-        if (esc_row(ent) == r && (c >> 4) == t) {
+      // the tile's escapes, four independent loads at a time
+      for (uint32_t e = e0; e < e1; e += 4) {
+        uint32_t ent[4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent);
+        for (int u = 0; u < 4; ++u) ent[u] = e + u < e1 ? esc[e + u] : 0xFFFFFFFFu;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = esc_col(ent[u]);
+          if (ent[u] != 0xFFFFFFFFu && esc_row(ent[u]) == r && (c >> 4) == t) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent[u]);
+          }
         }
       }
       const int64_t k0 = kc * kTileK + 16 * t;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (k0 + j < K) acc += (double)bf16f(xr[k0 + j]) * (double)bf16f(w[j]);
+        if (k0 + j < K) acc2(ah, al, __fmul_rn(bf16f(xr[k0 + j]), bf16f(w[j])));
     }
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (beats(acc, (int32_t)v, best.val, best.idx)) best = Best{acc, (int32_t)v};
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ah, o), ol = __shfl_xor_sync(0xFFFFFFFFu, al, o);
+      acc2(ah, al, oh);
+      al = __fadd_rn(al, ol);
+    }
+    if (lane == 0) {
+      shh[warp] = ah;
+      shl[warp] = al;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float h = shh[0], l = shl[0];
+      for (int w2 = 1; w2 < kExactWarps; ++w2) {
+        acc2(h, l, shh[w2]);
+        l = __fadd_rn(l, shl[w2]);
+      }
+      const double acc = (double)h + (double)l;
+      if (beats(acc, (int32_t)v, best.val, best.idx)) best = Best{acc, (int32_t)v};
+    }
+    __syncthreads();
   }
-  if (lane == 0) sh[warp] = best;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Best b = sh[0];
-    for (int w = 1; w < kExactWarps; ++w)
-      if (beats(sh[w].val, sh[w].idx, b.val, b.idx)) b = sh[w];
-    part[m * kExactBlocks + blockIdx.x] = b;
-  }
+  if (threadIdx.x == 0) part[m * gridDim.x + blockIdx.x] = best;
 }
 
-__global__ void k_cert_final(const Best* __restrict__ part, const int32_t* __restrict__ count, int32_t* __restrict__ tok,
-                             int32_t* __restrict__ ncand) {
+// One block of 256 per row: thread i merges partials i and i + 256, then the warps and
+// the block merge in a fixed order.
+__global__ void __launch_bounds__(256) k_cert_final(const Best* __restrict__ part, const int32_t* __restrict__ count,
+                                                    int32_t* __restrict__ tok, int32_t* __restrict__ ncand) {
+  __shared__ Best sh[8];
   const int64_t m = blockIdx.x;
-  if (threadIdx.x != 0) return;
-  Best b = part[m * kExactBlocks];
-  for (int i = 1; i < kExactBlocks; ++i) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Best b{0.0, -1};
+  for (int i = threadIdx.x; i < kExactBlocks; i += 256) {
     const Best c = part[m * kExactBlocks + i];
     if (beats(c.val, c.idx, b.val, b.idx)) b = c;
   }
-  tok[m] = b.idx;
-  if (ncand) ncand[m] = count[m];
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ov = __shfl_xor_sync(0xFFFFFFFFu, b.val, o);
+    const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, b.idx, o);
+    if (beats(ov, oi, b.val, b.idx)) b = Best{ov, oi};
+  }
+  if (lane == 0) sh[warp] = b;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w)
+      if (beats(sh[w].val, sh[w].idx, b.val, b.idx)) b = sh[w];
+    tok[m] = b.idx;
+    if (ncand) ncand[m] = count[m];
+  }
 }
 
 struct CertWs {
@@ -241,10 +307,9 @@ CertWs cert_ws(int64_t M, int64_t V, int64_t K) {
   off = al256(off + (size_t)M * (size_t)V * 4);
   L.nx = off;
   off = al256(off + (size_t)M * 4);
-  L.thr = off;
-  off = al256(off + (size_t)M * 4);
-  L.count = off;
-  off = al256(off + (size_t)M * 4);
+  L.thr = off;  // thr keys, then counts: zeroed by one memset
+  L.count = off + (size_t)M * 4;
+  off = al256(off + (size_t)M * 8);
   L.cand = off;
   off = al256(off + (size_t)M * (size_t)V * 4);
   L.part = off;
@@ -309,7 +374,7 @@ int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, con
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* lh = reinterpret_cast<float*>(w + L.lh);
   float* nx = reinterpret_cast<float*>(w + L.nx);
-  float* thr = reinterpret_cast<float*>(w + L.thr);
+  uint32_t* thr = reinterpret_cast<uint32_t*>(w + L.thr);
   int32_t* count = reinterpret_cast<int32_t*>(w + L.count);
   int32_t* cand = reinterpret_cast<int32_t*>(w + L.cand);
   Best* part = reinterpret_cast<Best*>(w + L.part);
@@ -317,16 +382,16 @@ int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, con
   if ((st = i8_gemm_impl(x, M, H->code, H->scale, V, K, lh, w + L.gemm, L.lh, s, fn))) return st;
   k_rownorm<<<(unsigned)M, 256, 0, s>>>(x, K, nx);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: row norms");
-  k_cert_thr<<<(unsigned)M, 1024, 0, s>>>(lh, V, nx, H->cbound, thr);
+  W12_CUDA_TRY(cudaMemsetAsync(thr, 0, (size_t)M * 8, s));
+  k_cert_thr<<<dim3(kThrBlocks, (unsigned)M), 1024, 0, s>>>(lh, V, nx, H->cbound, thr);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: threshold");
-  W12_CUDA_TRY(cudaMemsetAsync(count, 0, (size_t)M * 4, s));
   k_cert_cand<<<dim3((unsigned)((V + 1023) / 1024), (unsigned)M), 1024, 0, s>>>(lh, V, nx, H->cbound, thr, count, cand);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: candidates");
   k_cert_exact<<<dim3(kExactBlocks, (unsigned)M), kExactWarps * 32, 0, s>>>(
       x, K, KC, exact->hi, exact->lo, exact->base, exact->esc_tile_ptr, exact->esc, count, cand, V, W12_DECODE_MUL,
       part);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: exact logits");
-  k_cert_final<<<(unsigned)M, 32, 0, s>>>(part, count, tok, ncand);
+  k_cert_final<<<(unsigned)M, 256, 0, s>>>(part, count, tok, ncand);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: final");
   return W12_OK;
 }
