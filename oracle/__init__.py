@@ -73,6 +73,12 @@ def _L():
             lib.w12o_i8_quantize.restype = None
             lib.w12o_cert_argmax.argtypes = [p, i64, i64, p, i64, p, p, p, p, p]
             lib.w12o_cert_argmax.restype = i64
+            lib.w12o_split3.argtypes = [p, i64, p, p, p]
+            lib.w12o_split3.restype = None
+            lib.w12o_gdn_tree.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, p]
+            lib.w12o_gdn_tree.restype = ctypes.c_int
+            lib.w12o_gdn_commit.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
+            lib.w12o_gdn_commit.restype = None
             _lib = lib
         return _lib
 
@@ -296,3 +302,42 @@ def cert_argmax(x, W, code, scale, cbound, threads: int | None = None):
         with ThreadPoolExecutor(nt) as ex:
             list(ex.map(run, range(nt)))
     return idx, ncand
+
+
+def split3(x):
+    """Three bf16 pieces of each float (same page and section: the WY kernel holds the
+    FP32 state's 24-bit significand exactly in three BF16 pieces).  Returns bf16 bits
+    (s1, s2, s3), each the shape of x."""
+    x = _c(x, np.float32)
+    s1, s2, s3 = (np.empty(x.shape, np.uint16) for _ in range(3))
+    _L().w12o_split3(_p(x), x.size, _p(s1), _p(s2), _p(s3))
+    return s1, s2, s3
+
+
+def gdn_tree(S0, q, k, v, alpha, beta, parent):
+    """Gated-delta-rule outputs of every node of a draft tree (same page and section:
+    the path-verify kernel recomputes the recurrent state along each path).
+    S0 [H, dv, dk] float32; q, k [n, H, dk], v [n, H, dv] bf16 bits; alpha, beta [n, H]
+    float32; parent [n].  Returns O [n, H, dv] fp64, or None for an invalid tree."""
+    S0 = _c(S0, np.float32)
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    alpha, beta, parent = _c(alpha, np.float32), _c(beta, np.float32), _c(parent, np.int32)
+    H, dv, dk = S0.shape
+    n = parent.size
+    O = np.empty((n, H, dv), np.float64)
+    rc = _L().w12o_gdn_tree(_p(S0), _p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(parent), n, H, dk, dv, _p(O))
+    return None if rc != 0 else O
+
+
+def gdn_commit(S0, k, v, alpha, beta, nodes):
+    """State after replaying the accepted nodes (path order, root excluded) into S0
+    (same page and section: the commit kernel).  Returns S [H, dv, dk] fp64."""
+    S0 = _c(S0, np.float32)
+    k, v = _c(k, np.uint16), _c(v, np.uint16)
+    alpha, beta = _c(alpha, np.float32), _c(beta, np.float32)
+    L = len(nodes)
+    nodes = _c(np.asarray(nodes if L else [0]), np.int32)
+    H, dv, dk = S0.shape
+    S = np.empty((H, dv, dk), np.float64)
+    _L().w12o_gdn_commit(_p(S0), _p(k), _p(v), _p(alpha), _p(beta), _p(nodes), L, H, dk, dv, _p(S))
+    return S

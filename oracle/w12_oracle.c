@@ -449,3 +449,105 @@ int64_t w12o_cert_argmax(const uint16_t* x, int64_t M, int64_t K, const uint16_t
   free(hi);
   return total;
 }
+
+/* ---------------------------------------------------------------------------
+ * Hybrid-target recurrent verification (same page and section: for a target
+ * whose layers are mostly Gated DeltaNet, a path-verify kernel recomputes the
+ * recurrent state along each path instead of snapshotting it per node, a
+ * commit kernel replays the accepted path into the layers' states, and the
+ * WY kernel keeps the FP32 state as three BF16 pieces that hold its 24-bit
+ * significand exactly).  Readings where the sentence is silent:
+ *   - the recurrence is the gated delta rule on a d_v x d_k state:
+ *       S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *       o_t = S_t q_t,
+ *     per head, with q, k, v bf16 and alpha, beta float;
+ *   - a tree node's state is the root state S0 advanced by the updates of
+ *     every node on its path from the first draft node down to itself (node 0
+ *     is the committed root: its update is already in S0);
+ *   - the split of a float x is s1 = bf16_rne(x), s2 = bf16_rne(x - s1),
+ *     s3 = bf16_rne(x - s1 - s2), the differences taken in float.
+ * Arithmetic is fp64 (the split is float, as the reading states).
+ */
+static uint16_t bf16_rne_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static float bf16_float(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+void w12o_split3(const float* x, int64_t n, uint16_t* s1, uint16_t* s2, uint16_t* s3) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float a = x[i];
+    s1[i] = bf16_rne_bits(a);
+    const float r1 = a - bf16_float(s1[i]);
+    s2[i] = bf16_rne_bits(r1);
+    const float r2 = r1 - bf16_float(s2[i]);
+    s3[i] = bf16_rne_bits(r2);
+  }
+}
+
+/* One gated delta update of a dv x dk state (row-major S[v*dk + k]). */
+static void gdn_step(double* S, int64_t dk, int64_t dv, const uint16_t* k, const uint16_t* v, double alpha,
+                     double beta) {
+  for (int64_t r = 0; r < dv; ++r) {
+    double u = 0.0;
+    for (int64_t c = 0; c < dk; ++c) u += S[r * dk + c] * bf16_value(k[c]);
+    const double coef = beta * bf16_value(v[r]) - alpha * beta * u;
+    for (int64_t c = 0; c < dk; ++c) S[r * dk + c] = alpha * S[r * dk + c] + coef * bf16_value(k[c]);
+  }
+}
+
+/* Outputs of every node of a tree of n nodes for H heads.  S0[h*dv*dk] (float),
+ * q, k [n*H*dk], v [n*H*dv] (bf16), alpha, beta [n*H], parent[n] (parent[0] = -1,
+ * parent[i] < i).  O[(i*H + h)*dv + r] = (S_i q_i)[r].  Returns 0, or -1 for an
+ * invalid tree. */
+int w12o_gdn_tree(const float* S0, const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                  const float* beta, const int32_t* parent, int64_t n, int64_t H, int64_t dk, int64_t dv, double* O) {
+  if (n < 1 || parent[0] != -1) return -1;
+  for (int64_t i = 1; i < n; ++i)
+    if (parent[i] < 0 || parent[i] >= i) return -1;
+  double* S = (double*)malloc(sizeof(double) * (size_t)(dv * dk));
+  int64_t* path = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t L = 0;
+    for (int64_t j = i; j > 0; j = parent[j]) path[L++] = j;  /* node i up to the first draft node */
+    for (int64_t h = 0; h < H; ++h) {
+      for (int64_t e = 0; e < dv * dk; ++e) S[e] = (double)S0[h * dv * dk + e];
+      for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t j = path[t];
+        gdn_step(S, dk, dv, k + (j * H + h) * dk, v + (j * H + h) * dv, (double)alpha[j * H + h],
+                 (double)beta[j * H + h]);
+      }
+      for (int64_t r = 0; r < dv; ++r) {
+        double o = 0.0;
+        for (int64_t c = 0; c < dk; ++c) o += S[r * dk + c] * bf16_value(q[(i * H + h) * dk + c]);
+        O[(i * H + h) * dv + r] = o;
+      }
+    }
+  }
+  free(S);
+  free(path);
+  return 0;
+}
+
+/* Commit: the states after the accepted nodes nodes[0..L) (in path order, root
+ * excluded) are applied to S0 -> S_out[h*dv*dk], fp64. */
+void w12o_gdn_commit(const float* S0, const uint16_t* k, const uint16_t* v, const float* alpha, const float* beta,
+                     const int32_t* nodes, int64_t L, int64_t H, int64_t dk, int64_t dv, double* S_out) {
+  for (int64_t h = 0; h < H; ++h) {
+    double* S = S_out + h * dv * dk;
+    for (int64_t e = 0; e < dv * dk; ++e) S[e] = (double)S0[h * dv * dk + e];
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t j = nodes[t];
+      gdn_step(S, dk, dv, k + (j * H + h) * dk, v + (j * H + h) * dv, (double)alpha[j * H + h],
+               (double)beta[j * H + h]);
+    }
+  }
+}

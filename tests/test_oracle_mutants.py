@@ -5,7 +5,8 @@ The mutant is compiled on the CPU into a temporary library and the pin suite
 report a failure.  This shows the pins constrain every step of the oracle:
 window choice, record layout, planes, decode, the 8-bit view, the fp64 GEMM
 and its bound, argmax ties, tree acceptance, the two-level-verification splice, the
-node budget, and the INT8 head's quantizer, bound and certified argmax.
+node budget, the INT8 head's quantizer, bound and certified argmax, and the gated
+delta rule's path verify, commit and three-piece split.
 """
 import os
 import subprocess
@@ -64,6 +65,21 @@ MUTANTS = {
     "cert threshold uses the upper end": ("      if (lo[v] > thr) thr = lo[v];", "      if (hi[v] > thr) thr = hi[v];"),
     "cert keeps only the approximate argmax": ("      if (hi[v] < thr) continue;", "      if (hi[v] < thr || lo[v] < thr) continue;"),
     "cert ties go high": ("      if (best < 0 || better(L, best_val)) {", "      if (best < 0 || !better(best_val, L)) {"),
+    "split truncates": ("  u += 0x7FFFu + ((u >> 16) & 1u);\n  return (uint16_t)(u >> 16);\n}\n\nstatic float bf16_float",
+                        "  return (uint16_t)(u >> 16);\n}\n\nstatic float bf16_float"),
+    "split drops the third piece": ("    s3[i] = bf16_rne_bits(r2);", "    s3[i] = 0;"),
+    "gdn gate dropped": ("S[r * dk + c] = alpha * S[r * dk + c] + coef * bf16_value(k[c]);",
+                         "S[r * dk + c] = S[r * dk + c] + coef * bf16_value(k[c]);"),
+    "gdn erase not gated": ("const double coef = beta * bf16_value(v[r]) - alpha * beta * u;",
+                            "const double coef = beta * bf16_value(v[r]) - beta * u;"),
+    "gdn write sign flipped": ("const double coef = beta * bf16_value(v[r]) - alpha * beta * u;",
+                               "const double coef = -beta * bf16_value(v[r]) - alpha * beta * u;"),
+    "gdn path includes the root": ("for (int64_t j = i; j > 0; j = parent[j]) path[L++] = j;",
+                                   "for (int64_t j = i; j >= 0; j = parent[j]) path[L++] = j;"),
+    "gdn path applied backwards": ("      for (int64_t t = L - 1; t >= 0; --t) {\n        const int64_t j = path[t];",
+                                   "      for (int64_t t = 0; t < L; ++t) {\n        const int64_t j = path[t];"),
+    "gdn output reads the key": ("o += S[r * dk + c] * bf16_value(q[(i * H + h) * dk + c]);",
+                                 "o += S[r * dk + c] * bf16_value(k[(i * H + h) * dk + c]);"),
 }
 
 

@@ -623,3 +623,140 @@ def test_cert_argmax_all_zero_head_and_single_channel():
     code, scale, cb = oracle.i8_quantize(W1)
     idx, ncand = oracle.cert_argmax(x, W1, code, scale, cb)
     assert idx.tolist() == [0, 0] and ncand.tolist() == [1, 1]
+
+
+# ----------------------------------------------------------------------------- GDN path verify
+# Same page and section: for a hybrid target (most layers Gated DeltaNet) a path-verify
+# kernel recomputes the recurrent state along each draft path, a commit kernel replays the
+# accepted path, and the WY kernel holds the FP32 state in three BF16 pieces exactly.
+
+def test_split3_is_exact_and_first_piece_is_bf16_rne():
+    import torch
+    rng = np.random.default_rng(31)
+    e = rng.integers(-100, 127, 20000)
+    m = rng.random(20000) + 1.0
+    x = (np.sign(rng.random(20000) - 0.5) * m * 2.0 ** e).astype(np.float32)
+    x = np.concatenate([x, np.float32([0.0, -0.0, 1.0, -2.5, 1 + 2 ** -23, 3.0e38, 2.0 ** -100])])
+    s1, s2, s3 = oracle.split3(x)
+    v = [f32_of_bf16(s).astype(np.float64) for s in (s1, s2, s3)]
+    assert np.array_equal(v[0] + v[1] + v[2], x.astype(np.float64))
+    # the first piece is the library's round-to-nearest-even bf16 conversion
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(s1, ref)
+    # each further piece is at most half a unit in the last place of the one before
+    nz = v[0] != 0
+    assert (np.abs(v[1][nz]) <= np.abs(v[0][nz]) * 2.0 ** -8).all()
+    # a value that is already bf16 has empty further pieces
+    b = f32_of_bf16(s1)
+    t1, t2, t3 = oracle.split3(b)
+    assert np.array_equal(t1, s1) and not t2.any() and not t3.any()
+
+
+def gdn_inputs(rng, n, H, dk, dv, unit_k=True):
+    S0 = rng.standard_normal((H, dv, dk)).astype(np.float32) * 0.5
+    q = bf16_of_f32((rng.standard_normal((n, H, dk)) / np.sqrt(dk)).astype(np.float32))
+    kk = rng.standard_normal((n, H, dk))
+    if unit_k:
+        kk /= np.linalg.norm(kk, axis=2, keepdims=True)
+    k = bf16_of_f32(kk.astype(np.float32))
+    v = bf16_of_f32(rng.standard_normal((n, H, dv)).astype(np.float32))
+    alpha = rng.uniform(0.85, 1.0, (n, H)).astype(np.float32)
+    beta = rng.uniform(0.1, 0.9, (n, H)).astype(np.float32)
+    return S0, q, k, v, alpha, beta
+
+
+def random_tree(rng, n):
+    return np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+
+
+def depth_of(parent):
+    d = np.zeros(len(parent), np.int64)
+    for i in range(1, len(parent)):
+        d[i] = d[parent[i]] + 1
+    return d
+
+
+def test_gdn_no_write_is_the_gated_decay_of_s0():
+    """beta = 0: no rank-1 writes, so node i reads (product of alpha on its path) * S0 q_i;
+    alpha = 1 as well leaves S0 q_i."""
+    rng = np.random.default_rng(32)
+    n, H, dk, dv = 12, 2, 16, 8
+    S0, q, k, v, alpha, beta = gdn_inputs(rng, n, H, dk, dv)
+    parent = random_tree(rng, n)
+    beta[:] = 0
+    O = oracle.gdn_tree(S0, q, k, v, alpha, beta, parent)
+    qf = f32_of_bf16(q).astype(np.float64)
+    base = np.einsum("hvk,nhk->nhv", S0.astype(np.float64), qf)
+    decay = np.ones((n, H))
+    for i in range(1, n):
+        decay[i] = decay[parent[i]] * alpha[i].astype(np.float64)
+    assert np.allclose(O, base * decay[:, :, None], rtol=1e-12, atol=1e-12)
+    alpha[:] = 1
+    assert np.allclose(oracle.gdn_tree(S0, q, k, v, alpha, beta, parent), base, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("a", [1.0, 0.75])
+def test_gdn_delta_rule_overwrites_the_key_column(a):
+    """k = e_j, beta = 1, alpha = a: the update erases the decayed column j and writes v
+    there, so a query e_j reads v exactly and a query e_m (m != j) reads a * S0's
+    column m."""
+    rng = np.random.default_rng(33)
+    H, dk, dv = 3, 8, 6
+    S0, q, k, v, alpha, beta = gdn_inputs(rng, 2, H, dk, dv)
+    parent = np.array([-1, 0], np.int32)
+    alpha[:] = a
+    beta[:] = 1
+    j, mcol = 3, 5
+    k[:] = 0
+    k[1, :, j] = 0x3F80                   # e_j
+    for col, expect in ((j, f32_of_bf16(v[1]).astype(np.float64)), (mcol, a * S0[:, :, mcol].astype(np.float64))):
+        q[:] = 0
+        q[1, :, col] = 0x3F80
+        O = oracle.gdn_tree(S0, q, k, v, alpha, beta, parent)
+        assert np.array_equal(O[1], expect)
+
+
+def test_gdn_tree_node_equals_its_path_as_a_chain():
+    rng = np.random.default_rng(34)
+    n, H, dk, dv = 10, 2, 16, 16
+    S0, q, k, v, alpha, beta = gdn_inputs(rng, n, H, dk, dv)
+    parent = random_tree(rng, n)
+    O = oracle.gdn_tree(S0, q, k, v, alpha, beta, parent)
+    for i in range(n):
+        path = []
+        j = i
+        while j >= 0:
+            path.append(j)
+            j = parent[j]
+        path = path[::-1]                        # root .. i
+        L = len(path)
+        chain = np.arange(-1, L - 1, dtype=np.int32)
+        Oc = oracle.gdn_tree(S0, q[path], k[path], v[path], alpha[path], beta[path], chain)
+        assert np.array_equal(Oc[L - 1], O[i])
+
+
+def test_gdn_commit_then_read_equals_the_tree_output():
+    """Replaying a path into the state and then reading with node i's query gives node i's
+    tree output; an empty commit leaves S0."""
+    rng = np.random.default_rng(35)
+    n, H, dk, dv = 9, 2, 16, 12
+    S0, q, k, v, alpha, beta = gdn_inputs(rng, n, H, dk, dv)
+    parent = random_tree(rng, n)
+    O = oracle.gdn_tree(S0, q, k, v, alpha, beta, parent)
+    i = int(np.argmax(depth_of(parent)))
+    path = []
+    j = i
+    while j > 0:
+        path.append(j)
+        j = parent[j]
+    S = oracle.gdn_commit(S0, k, v, alpha, beta, path[::-1])
+    read = np.einsum("hvk,hk->hv", S, f32_of_bf16(q[i]).astype(np.float64))
+    assert np.allclose(read, O[i], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.gdn_commit(S0, k, v, alpha, beta, []), S0.astype(np.float64))
+
+
+def test_gdn_rejects_invalid_trees():
+    rng = np.random.default_rng(36)
+    S0, q, k, v, alpha, beta = gdn_inputs(rng, 3, 1, 4, 4)
+    for bad in ([0, 0, 1], [-1, 1, 0], [-1, 0, 3]):
+        assert oracle.gdn_tree(S0, q, k, v, alpha, beta, np.array(bad, np.int32)) is None
