@@ -753,6 +753,60 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
     out["cert_head_m16"] = cert
     del Hc, Ac
     torch.cuda.empty_cache()
+
+    # ---- recurrent layers of a hybrid target: 48 gated-delta-rule layers, 32 heads of
+    # 128 x 128 float state, a 32-node draft tree.  One step: path verify of every node on
+    # every layer, then the commit of the accepted path (the same four nodes) into every
+    # layer's state.  Per-node state snapshots would hold n x H x dv x dk floats per layer.
+    n_l, Hg, dg, nn = 48, 32, 128, 32
+    rg = np.random.default_rng(48)
+    par_g = torch.from_numpy(np.array([-1] + [int(rg.integers(max(0, i - 4), i)) for i in range(1, nn)],
+                                      np.int32)).to(dev)
+
+    def bf16_dev(a):
+        u = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+        return torch.from_numpy(((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16).view(np.int16)).to(dev)
+
+    layers_g = []
+    for _ in range(n_l):
+        kk = rg.standard_normal((nn, Hg, dg))
+        layers_g.append(dict(
+            S=torch.from_numpy((rg.standard_normal((Hg, dg, dg)) * 0.5).astype(np.float32)).to(dev),
+            q=bf16_dev(rg.standard_normal((nn, Hg, dg)) / np.sqrt(dg)),
+            k=bf16_dev(kk / np.linalg.norm(kk, axis=2, keepdims=True)),
+            v=bf16_dev(rg.standard_normal((nn, Hg, dg))),
+            a=torch.from_numpy(rg.uniform(0.85, 1.0, (nn, Hg)).astype(np.float32)).to(dev),
+            b=torch.from_numpy(rg.uniform(0.1, 0.9, (nn, Hg)).astype(np.float32)).to(dev),
+            O=torch.empty((nn, Hg, dg), dtype=torch.float32, device=dev)))
+    acc_nodes = [0]
+    while len(acc_nodes) < 5:                      # a path of four accepted draft nodes
+        kids = [i for i in range(nn) if int(par_g[i]) == acc_nodes[-1]]
+        if not kids:
+            break
+        acc_nodes.append(kids[0])
+    pn = torch.zeros(nn, dtype=torch.int32, device=dev)
+    pn[:len(acc_nodes)] = torch.tensor(acc_nodes, dtype=torch.int32)
+    pl = torch.tensor([len(acc_nodes) - 1], dtype=torch.int32, device=dev)
+    st_g = torch.zeros(1, dtype=torch.int32, device=dev)
+    S_keep = [Lg["S"].clone() for Lg in layers_g]
+
+    def gdn_verify_all():
+        for Lg in layers_g:
+            w12.gdn_path_verify(Lg["S"], Lg["q"], Lg["k"], Lg["v"], Lg["a"], Lg["b"], par_g, O=Lg["O"], status=st_g)
+
+    def gdn_commit_all():
+        for Lg in layers_g:
+            w12.gdn_commit(Lg["S"], Lg["k"], Lg["v"], Lg["a"], Lg["b"], pl, pn, status=st_g)
+
+    ms_v = timed_ms(torch, gdn_verify_all, steps)
+    ms_c = timed_ms(torch, gdn_commit_all, steps)      # each call advances the states further
+    for Lg, S0g in zip(layers_g, S_keep):
+        Lg["S"].copy_(S0g)
+    out["gdn_verify_48x32"] = {"layers": n_l, "heads": Hg, "dk": dg, "dv": dg, "tree_nodes": nn,
+                               "accepted": len(acc_nodes) - 1, "path_verify_us": 1e3 * ms_v,
+                               "commit_us": 1e3 * ms_c, "step_us": 1e3 * (ms_v + ms_c),
+                               "snapshot_bytes_avoided": n_l * nn * Hg * dg * dg * 4,
+                               "status": int(st_g.item())}
     return out
 
 

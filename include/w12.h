@@ -330,6 +330,44 @@ W12_API size_t w12_cert_head_workspace_size(int64_t M, int64_t V, int64_t K);
 W12_API int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, const w12_matrix* exact,
                                  int32_t* tok, int32_t* ncand, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Recurrent layers of a hybrid target.  The SpecPilot summary page, section
+ * "What's different", verifies a draft tree on a target whose layers are
+ * mostly Gated DeltaNet with a path-verify kernel (the recurrent state is
+ * recomputed along each path instead of snapshotted per node), a commit kernel
+ * (the accepted path is replayed into the state) and FP32 state held exactly
+ * as three BF16 pieces.  Recurrence per head, state S (dv x dk, row-major
+ * float), q, k (dk) and v (dv) bf16, alpha and beta float:
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t.
+ * dk, dv <= 256 with (dk * (dv + 1) + dk + dv) * 4 <= 200 KB (W12_ERR_SHAPE
+ * otherwise).
+ */
+
+/* s1 = bf16_rne(x), s2 = bf16_rne(x - s1), s3 = bf16_rne(x - s1 - s2) (float
+ * differences) for n floats; s1 + s2 + s3 == x exactly when no piece overflows
+ * bf16 and |x| >= 2^-110 (or x = 0). */
+W12_API int gdn_split3(const float* x, int64_t n, uint16_t* s1, uint16_t* s2, uint16_t* s3, void* stream);
+
+/* Outputs of every node of an n-node draft tree (parent[0] = -1, parent[i] <
+ * i; node 0 is the committed root, whose update is already in S0):
+ * O[(i*H + h)*dv + r] = (S_i q_i)[r], S_i = S0[h] advanced by the updates of
+ * the nodes on i's path below the root, root side first.  q, k [n*H*dk], v
+ * [n*H*dv], alpha, beta [n*H], S0 [H*dv*dk].  A malformed tree sets bit 0 of
+ * *status (device int32, zeroed by the caller) and leaves O unwritten.
+ * n in 1..4096. */
+W12_API int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            const float* alpha, const float* beta, const int32_t* parent, int64_t n, int64_t H,
+                            int64_t dk, int64_t dv, float* O, int32_t* status, void* stream);
+
+/* S[h] <- S[h] advanced by the accepted nodes path_nodes[1 .. *path_len] (device
+ * values, as w12_lmhead_verify writes them: path_nodes[0] is the root), in
+ * order; node inputs as for gdn_path_verify.  *path_len <= 0 commits nothing;
+ * a length >= n or a node outside 1..n-1 sets bit 1 of *status and leaves S. */
+W12_API int gdn_commit(float* S, const uint16_t* k, const uint16_t* v, const float* alpha, const float* beta,
+                       const int32_t* path_len, const int32_t* path_nodes, int64_t n, int64_t H, int64_t dk,
+                       int64_t dv, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,6 +80,9 @@ SIGNATURES = [
     ("w12_i8_encode", ctypes.c_int, [_P, ctypes.POINTER(w12_i8_head), _P]),
     ("w12_cert_head_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w12_cert_head_argmax", ctypes.c_int, [_P, _I64, ctypes.POINTER(w12_i8_head), _MP, _P, _P, _P, _SZ, _P]),
+    ("gdn_split3", ctypes.c_int, [_P, _I64, _P, _P, _P, _P]),
+    ("gdn_path_verify", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
+    ("gdn_commit", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P]),
 ]
 
 
@@ -435,3 +438,48 @@ def w12_cert_head_argmax(x: torch.Tensor, H: I8Head, exact: W12Matrix, tok: torc
     _check(lib().w12_cert_head_argmax(_ptr(x), M, H.desc(), exact.desc(), _ptr(tok), _ptr(ncand), _ptr(buf),
                                       buf.numel(), _stream(stream)))
     return tok, ncand
+
+
+# ---------------------------------------------------------------- recurrent layers (gated delta rule)
+
+def _f32(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous float32 CUDA tensor")
+    return t
+
+
+def gdn_split3(x: torch.Tensor, stream=None):
+    """Three bf16 pieces (bits as int16) of each float of x: s1 + s2 + s3 == x."""
+    x = _f32(x)
+    s = [torch.empty(x.shape, dtype=torch.int16, device=x.device) for _ in range(3)]
+    _check(lib().gdn_split3(_ptr(x), x.numel(), _ptr(s[0]), _ptr(s[1]), _ptr(s[2]), _stream(stream)))
+    return tuple(s)
+
+
+def gdn_path_verify(S0, q, k, v, alpha, beta, parent, O=None, status=None, stream=None):
+    """Outputs O [n, H, dv] of every node of a draft tree under the gated delta rule
+    (state recomputed along each path).  S0 [H, dv, dk] float32; q, k [n, H, dk], v [n, H, dv]
+    bf16 bits; alpha, beta [n, H] float32; parent [n] int32.  Returns (O, status)."""
+    S0, alpha, beta = _f32(S0), _f32(alpha), _f32(beta)
+    q, k, v, parent = _bits16(q), _bits16(k), _bits16(v), _i32(parent)
+    H, dv, dk = S0.shape
+    n = parent.numel()
+    O = torch.empty((n, H, dv), dtype=torch.float32, device=S0.device) if O is None else _f32(O)
+    status = torch.zeros(1, dtype=torch.int32, device=S0.device) if status is None else _i32(status)
+    _check(lib().gdn_path_verify(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(parent), n, H, dk,
+                                 dv, _ptr(O), _ptr(status), _stream(stream)))
+    return O, status
+
+
+def gdn_commit(S, k, v, alpha, beta, path_len, path_nodes, status=None, stream=None):
+    """S [H, dv, dk] float32, in place: advanced by the accepted nodes path_nodes[1..path_len]
+    (device int32 tensors as w12_lmhead_verify returns them).  Returns status."""
+    S, alpha, beta = _f32(S), _f32(alpha), _f32(beta)
+    k, v = _bits16(k), _bits16(v)
+    path_len, path_nodes = _i32(path_len), _i32(path_nodes)
+    H, dv, dk = S.shape
+    n = alpha.shape[0]
+    status = torch.zeros(1, dtype=torch.int32, device=S.device) if status is None else _i32(status)
+    _check(lib().gdn_commit(_ptr(S), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(path_len), _ptr(path_nodes), n, H,
+                            dk, dv, _ptr(status), _stream(stream)))
+    return status
