@@ -219,6 +219,197 @@ __global__ void k_gdn_commit(float* __restrict__ S_io, const uint16_t* __restric
   gdn_store(S_io + h * dv * dk, dk, dv, S);
 }
 
+// ---- register-resident state for dk = 64 and 128.  The rows of a state evolve
+// independently (they share only k and v), so a block takes 32 rows: thread
+// (r = t/4, p = t%4) of the 128 keeps columns [p*Q, p*Q + Q) of row r0 + r in registers
+// (Q = DK/4); k, v and q go through shared memory with each quarter of k padded by 4
+// floats (the four quarters on distinct banks).
+constexpr int kRegRows = 32;
+constexpr int kRegThreads = 4 * kRegRows;
+
+template <int DK>
+struct RegState {
+  static constexpr int Q = DK / 4;
+  float s[Q];
+};
+
+template <int DK>
+__device__ __forceinline__ void reg_load(RegState<DK>& S, const float* __restrict__ src, int64_t rows) {
+  const int64_t r = threadIdx.x >> 2;
+  const int p = threadIdx.x & 3;
+  if (r < rows) {
+    const float4* g = reinterpret_cast<const float4*>(src + r * DK + p * RegState<DK>::Q);
+#pragma unroll
+    for (int m = 0; m < RegState<DK>::Q / 4; ++m) {
+      const float4 f = g[m];
+      S.s[4 * m] = f.x;
+      S.s[4 * m + 1] = f.y;
+      S.s[4 * m + 2] = f.z;
+      S.s[4 * m + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < RegState<DK>::Q; ++m) S.s[m] = 0.f;
+  }
+}
+
+template <int DK>
+__device__ __forceinline__ void reg_store(const RegState<DK>& S, float* __restrict__ dst, int64_t rows) {
+  const int64_t r = threadIdx.x >> 2;
+  const int p = threadIdx.x & 3;
+  if (r < rows) {
+    float4* g = reinterpret_cast<float4*>(dst + r * DK + p * RegState<DK>::Q);
+#pragma unroll
+    for (int m = 0; m < RegState<DK>::Q / 4; ++m)
+      g[m] = make_float4(S.s[4 * m], S.s[4 * m + 1], S.s[4 * m + 2], S.s[4 * m + 3]);
+  }
+}
+
+// padded position of element c of k (or q) in shared memory
+template <int DK>
+__device__ __forceinline__ int vpos(int c) {
+  return c + (c / RegState<DK>::Q) * 4;
+}
+
+template <int DK>
+__device__ __forceinline__ float reg_dot(const RegState<DK>& S, const float* vec) {
+  constexpr int Q = RegState<DK>::Q;
+  const float4* v4 = reinterpret_cast<const float4*>(vec + (threadIdx.x & 3) * (Q + 4));
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < Q / 4; ++m) {
+    const float4 f = v4[m];
+    a0 = fmaf(S.s[4 * m], f.x, a0);
+    a1 = fmaf(S.s[4 * m + 1], f.y, a1);
+    a0 = fmaf(S.s[4 * m + 2], f.z, a0);
+    a1 = fmaf(S.s[4 * m + 3], f.w, a1);
+  }
+  float u = a0 + a1;
+  u += __shfl_xor_sync(0xFFFFFFFFu, u, 1);
+  u += __shfl_xor_sync(0xFFFFFFFFu, u, 2);
+  return u;
+}
+
+// One step's inputs: k element t (t < DK), v of row r0 + t (t < 32), alpha, beta.
+template <int DK>
+__device__ __forceinline__ StepIn fetch_rows(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                             const float* __restrict__ alpha, const float* __restrict__ beta,
+                                             int64_t j, int64_t h, int64_t H, int64_t dv, int64_t r0) {
+  StepIn in;
+  const int64_t t = threadIdx.x;
+  in.k = t < DK ? bf16v(k[(j * H + h) * DK + t]) : 0.f;
+  in.v = t < kRegRows && r0 + t < dv ? bf16v(v[(j * H + h) * dv + r0 + t]) : 0.f;
+  in.alpha = alpha[j * H + h];
+  in.beta = beta[j * H + h];
+  return in;
+}
+
+// kv: k (padded, 4*(Q+4) floats) then the block's 32 v values
+template <int DK>
+__device__ __forceinline__ void reg_step(RegState<DK>& S, float* kv, const StepIn& in) {
+  constexpr int Q = RegState<DK>::Q;
+  __syncthreads();  // the previous step's reads of kv are done
+  if (threadIdx.x < DK) kv[vpos<DK>(threadIdx.x)] = in.k;
+  if (threadIdx.x < kRegRows) kv[4 * (Q + 4) + threadIdx.x] = in.v;
+  __syncthreads();
+  const float u = reg_dot<DK>(S, kv);
+  const float coef = in.beta * kv[4 * (Q + 4) + (threadIdx.x >> 2)] - in.alpha * in.beta * u;
+  const float4* k4 = reinterpret_cast<const float4*>(kv + (threadIdx.x & 3) * (Q + 4));
+#pragma unroll
+  for (int m = 0; m < Q / 4; ++m) {
+    const float4 f = k4[m];
+    S.s[4 * m] = fmaf(in.alpha, S.s[4 * m], coef * f.x);
+    S.s[4 * m + 1] = fmaf(in.alpha, S.s[4 * m + 1], coef * f.y);
+    S.s[4 * m + 2] = fmaf(in.alpha, S.s[4 * m + 2], coef * f.z);
+    S.s[4 * m + 3] = fmaf(in.alpha, S.s[4 * m + 3], coef * f.w);
+  }
+}
+
+// grid (node, head, row block of 32)
+template <int DK>
+__global__ void __launch_bounds__(kRegThreads) k_gdn_path_verify_reg(
+    const float* __restrict__ S0, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const uint16_t* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
+    const int32_t* __restrict__ parent, int64_t n, int64_t H, int64_t dv, float* __restrict__ O,
+    int32_t* __restrict__ status) {
+  constexpr int Q = RegState<DK>::Q;
+  __shared__ __align__(16) float kv[4 * (Q + 4) + kRegRows];
+  __shared__ int32_t path[kGdnMaxNodes];
+  __shared__ int32_t plen;
+  const int64_t i = blockIdx.x, h = blockIdx.y, r0 = (int64_t)blockIdx.z * kRegRows;
+  if (threadIdx.x == 0) {
+    int32_t L = 0;
+    bool ok = parent[0] == -1;
+    for (int64_t j = i; ok && j > 0;) {
+      const int32_t p = parent[j];
+      if (p < 0 || p >= j) {
+        ok = false;
+        break;
+      }
+      path[L++] = (int32_t)j;
+      j = p;
+    }
+    if (!ok) {
+      if (blockIdx.z == 0) atomicOr(status, 1);
+      L = -1;
+    }
+    plen = L;
+  }
+  RegState<DK> S;
+  reg_load<DK>(S, S0 + (h * dv + r0) * DK, dv - r0);
+  __syncthreads();
+  const int32_t L = plen;
+  if (L < 0) return;
+  StepIn in{};
+  if (L > 0) in = fetch_rows<DK>(k, v, alpha, beta, path[L - 1], h, H, dv, r0);
+  const float qx = threadIdx.x < DK ? bf16v(q[(i * H + h) * DK + threadIdx.x]) : 0.f;
+  for (int32_t t = L - 1; t >= 0; --t) {
+    const StepIn cur = in;
+    if (t > 0) in = fetch_rows<DK>(k, v, alpha, beta, path[t - 1], h, H, dv, r0);
+    reg_step<DK>(S, kv, cur);
+  }
+  __syncthreads();
+  if (threadIdx.x < DK) kv[vpos<DK>(threadIdx.x)] = qx;
+  __syncthreads();
+  const float o = reg_dot<DK>(S, kv);
+  const int64_t r = r0 + (threadIdx.x >> 2);
+  if (r < dv && (threadIdx.x & 3) == 0) O[(i * H + h) * dv + r] = o;
+}
+
+// grid (head, row block of 32)
+template <int DK>
+__global__ void __launch_bounds__(kRegThreads) k_gdn_commit_reg(
+    float* __restrict__ S_io, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+    const float* __restrict__ alpha, const float* __restrict__ beta, const int32_t* __restrict__ path_len,
+    const int32_t* __restrict__ path_nodes, int64_t n, int64_t H, int64_t dv, int32_t* __restrict__ status) {
+  constexpr int Q = RegState<DK>::Q;
+  __shared__ __align__(16) float kv[4 * (Q + 4) + kRegRows];
+  const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kRegRows;
+  const int32_t L = *path_len;
+  if (L <= 0) return;
+  if (L >= n) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, 2);
+    return;
+  }
+  for (int32_t t = 1; t <= L; ++t) {
+    const int32_t j = path_nodes[t];
+    if (j <= 0 || j >= n) {
+      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, 2);
+      return;
+    }
+  }
+  RegState<DK> S;
+  float* base = S_io + (h * dv + r0) * DK;
+  reg_load<DK>(S, base, dv - r0);
+  StepIn in = fetch_rows<DK>(k, v, alpha, beta, path_nodes[1], h, H, dv, r0);
+  for (int32_t t = 1; t <= L; ++t) {
+    const StepIn cur = in;
+    if (t < L) in = fetch_rows<DK>(k, v, alpha, beta, path_nodes[t + 1], h, H, dv, r0);
+    reg_step<DK>(S, kv, cur);
+  }
+  reg_store<DK>(S, base, dv - r0);
+}
+
 // four threads per state row and a thread per element of k, whole warps
 int gdn_threads(int64_t dk, int64_t dv) {
   const int64_t t = 4 * dv > dk ? 4 * dv : dk;
@@ -274,6 +465,19 @@ int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* k, const
     return fail(W12_ERR_SHAPE, "%s: n=%lld out of range (1..%lld)", fn, (long long)n, (long long)kGdnMaxNodes);
   if (!S0 || !q || !k || !v || !alpha || !beta || !parent || !O || !status)
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
+  const bool aligned = (((uintptr_t)S0) & 15u) == 0;
+  if (aligned && (dk == 128 || dk == 64)) {  // state in registers, 32 rows a block
+    const dim3 grid((unsigned)n, (unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
+    const int threads = kRegThreads;
+    if (dk == 128)
+      k_gdn_path_verify_reg<128><<<grid, threads, 0, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
+                                                                             dv, O, status);
+    else
+      k_gdn_path_verify_reg<64><<<grid, threads, 0, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
+                                                                            dv, O, status);
+    W12_LAUNCH_CHECK(fn);
+    return W12_OK;
+  }
   const size_t smem = gdn_smem(dk, dv);
   if ((st = set_gdn_smem((const void*)k_gdn_path_verify, smem))) return st;
   k_gdn_path_verify<<<dim3((unsigned)n, (unsigned)H), gdn_threads(dk, dv), smem, (cudaStream_t)stream>>>(
@@ -291,6 +495,17 @@ int gdn_commit(float* S, const uint16_t* k, const uint16_t* v, const float* alph
   if (n < 1) return fail(W12_ERR_SHAPE, "%s: n=%lld", fn, (long long)n);
   if (!S || !k || !v || !alpha || !beta || !path_len || !path_nodes || !status)
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if ((((uintptr_t)S) & 15u) == 0 && (dk == 128 || dk == 64)) {  // state in registers, 32 rows a block
+    const dim3 grid((unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
+    if (dk == 128)
+      k_gdn_commit_reg<128><<<grid, kRegThreads, 0, (cudaStream_t)stream>>>(S, k, v, alpha, beta, path_len, path_nodes,
+                                                                           n, H, dv, status);
+    else
+      k_gdn_commit_reg<64><<<grid, kRegThreads, 0, (cudaStream_t)stream>>>(S, k, v, alpha, beta, path_len, path_nodes,
+                                                                          n, H, dv, status);
+    W12_LAUNCH_CHECK(fn);
+    return W12_OK;
+  }
   const size_t smem = gdn_smem(dk, dv);
   if ((st = set_gdn_smem((const void*)k_gdn_commit, smem))) return st;
   k_gdn_commit<<<(unsigned)H, gdn_threads(dk, dv), smem, (cudaStream_t)stream>>>(S, k, v, alpha, beta, path_len,

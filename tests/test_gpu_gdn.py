@@ -74,7 +74,8 @@ def test_split3_matches_oracle(w12):
 
 
 @pytest.mark.parametrize("n,H,dk,dv,chain", [(1, 1, 16, 16, False), (5, 3, 64, 32, False), (32, 2, 128, 128, False),
-                                             (12, 2, 48, 80, True), (40, 1, 96, 64, False)])
+                                             (12, 2, 48, 80, True), (40, 1, 96, 64, False), (9, 2, 64, 100, False),
+                                             (7, 2, 128, 200, False), (6, 1, 128, 1, True)])
 def test_path_verify_matches_oracle(w12, n, H, dk, dv, chain):
     rng = np.random.default_rng(n * 7 + H)
     S0, q, k, v, alpha, beta = inputs(rng, n, H, dk, dv)
@@ -104,10 +105,11 @@ def test_path_verify_flags_invalid_trees(w12):
         assert int(status.item()) & 1
 
 
-@pytest.mark.parametrize("L", [0, 1, 3])
-def test_commit_matches_oracle(w12, L):
-    rng = np.random.default_rng(44 + L)
-    n, H, dk, dv = 16, 4, 128, 64
+@pytest.mark.parametrize("L,dk,dv", [(0, 128, 64), (1, 128, 64), (3, 128, 64), (3, 64, 128), (2, 96, 40),
+                                     (3, 128, 160)])
+def test_commit_matches_oracle(w12, L, dk, dv):
+    rng = np.random.default_rng(44 + L + dk + dv)
+    n, H = 16, 4
     S0, q, k, v, alpha, beta = inputs(rng, n, H, dk, dv)
     nodes = [int(j) for j in rng.choice(np.arange(1, n), L, replace=False)]
     path_nodes = np.zeros(n, np.int32)
