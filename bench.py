@@ -58,7 +58,7 @@ def parse_args():
     p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack rows (32 GB of W12)")
-    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead", "cert"], default=None,
+    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead", "cert", "gdn"], default=None,
                    help="profiling case: repeat one matrix's GEMM (or the LM head) and print its time")
     p.add_argument("--q8", action="store_true", help="with --only: the 8-bit-view GEMM")
     return p.parse_args()
@@ -74,6 +74,53 @@ def run_only(args):
 
     torch.cuda.set_device(0)
     M = args.M
+    if args.only == "gdn":
+        # path verify of a 32-node tree and the commit of four accepted nodes on one
+        # gated-delta-rule layer of 32 heads of 128 x 128 state
+        nn, Hg, dg = 32, 32, 128
+        rg = np.random.default_rng(48)
+        par = torch.from_numpy(np.array([-1] + [int(rg.integers(max(0, i - 4), i)) for i in range(1, nn)],
+                                        np.int32)).cuda()
+
+        def bf16_dev(a):
+            u = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+            return torch.from_numpy(((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16).view(np.int16)).cuda()
+
+        kk = rg.standard_normal((nn, Hg, dg))
+        S = torch.from_numpy((rg.standard_normal((Hg, dg, dg)) * 0.5).astype(np.float32)).cuda()
+        q = bf16_dev(rg.standard_normal((nn, Hg, dg)) / np.sqrt(dg))
+        k = bf16_dev(kk / np.linalg.norm(kk, axis=2, keepdims=True))
+        v = bf16_dev(rg.standard_normal((nn, Hg, dg)))
+        al = torch.from_numpy(rg.uniform(0.85, 1.0, (nn, Hg)).astype(np.float32)).cuda()
+        be = torch.from_numpy(rg.uniform(0.1, 0.9, (nn, Hg)).astype(np.float32)).cuda()
+        O = torch.empty((nn, Hg, dg), dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pn = torch.zeros(nn, dtype=torch.int32, device="cuda")
+        node = 0
+        for t in range(1, 5):
+            kids = [i for i in range(nn) if int(par[i]) == node]
+            if not kids:
+                break
+            node = kids[0]
+            pn[t] = node
+        pl = torch.tensor([int((pn > 0).sum())], dtype=torch.int32, device="cuda")
+
+        def step():
+            w12.gdn_path_verify(S, q, k, v, al, be, par, O=O, status=st)
+            w12.gdn_commit(S, k, v, al, be, pl, pn, status=st)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"only": "gdn", "us_per_layer": 1e3 * a.elapsed_time(b) / args.steps,
+                          "status": int(st.item())}), flush=True)
+        return
     if args.only == "cert":
         # certified INT8 head on the head recipe, M rows pointing at random tokens
         V, K = LMHEAD
