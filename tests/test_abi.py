@@ -56,3 +56,33 @@ def test_argument_errors_are_reported_without_device_work():
     assert lib.tree_verify_tokens(None, None, None, None, 1, 4, None, None, None, None) == 1
     p = ctypes.c_void_p(256)
     assert lib.tree_verify_tokens(p, p, p, None, 2, 4, p, p, p, None) == 1   # several requests need offsets
+
+
+def test_certified_head_and_recurrent_argument_errors():
+    """The INT8 head and recurrent-layer calls check shapes and pointers on the host."""
+    import ctypes
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    p = ctypes.c_void_p(256)
+    assert lib.w12_i8_code_bytes(5120, 5120) == lib.w12_hi_bytes(5120, 5120)
+    assert lib.w12_cert_head_workspace_size(0, 10, 10) == 0
+    assert lib.w12_cert_head_workspace_size(16, 151936, 5120) > 16 * 151936 * 8
+    H = w12.w12_i8_head(0, 5120, 256, 256, 256)
+    assert lib.w12_i8_encode(p, ctypes.byref(H), None) == 2                      # V = 0
+    H = w12.w12_i8_head(8, 64, 264, 256, 256)
+    assert lib.w12_i8_encode(p, ctypes.byref(H), None) == 1                      # misaligned codes
+    assert b"aligned" in lib.w12_last_error()
+    H = w12.w12_i8_head(8, 64, 256, 256, 256)
+    A = w12.w12_matrix(8, 32, 256, 256, 256, 256, 0, 0)                          # K differs
+    assert lib.w12_cert_head_argmax(p, 4, ctypes.byref(H), ctypes.byref(A), p, None, p, 1 << 30, None) == 2
+    A = w12.w12_matrix(8, 64, 256, 256, 256, 256, 0, 0)
+    assert lib.w12_cert_head_argmax(p, 4, ctypes.byref(H), ctypes.byref(A), p, None, p, 16, None) == 3
+    # recurrent layers: dims, tree size, pointers
+    assert lib.gdn_split3(None, 0, None, None, None, None) == 0                  # nothing to do
+    assert lib.gdn_split3(None, 4, None, None, None, None) == 1
+    assert lib.gdn_path_verify(p, p, p, p, p, p, p, 4, 2, 256, 256, p, p, None) == 2   # state too large
+    assert b"shared memory" in lib.w12_last_error()
+    assert lib.gdn_path_verify(p, p, p, p, p, p, p, 5000, 2, 128, 128, p, p, None) == 2  # too many nodes
+    assert lib.gdn_path_verify(p, p, p, p, p, p, None, 4, 2, 128, 128, p, p, None) == 1
+    assert lib.gdn_commit(p, p, p, p, p, p, p, 0, 2, 128, 128, p, None) == 2
+    assert lib.gdn_commit(p, p, p, p, p, None, p, 4, 2, 128, 128, p, None) == 1
