@@ -360,6 +360,17 @@ W12_API int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* 
                             const float* alpha, const float* beta, const int32_t* parent, int64_t n, int64_t H,
                             int64_t dk, int64_t dv, float* O, int32_t* status, void* stream);
 
+/* The same outputs as gdn_path_verify in the WY form: node t's state is
+ * gamma_t S0 + sum_{j on path(t)} (gamma_t/gamma_j) d_j k_j^T (gamma: product of
+ * alpha along the path), whose pseudo-values d_j solve a triangular system over
+ * the tree; the state enters only through S0 k_t and S0 q_t, so every node is
+ * computed once instead of once per path that reaches it.  dk = 64 or 128,
+ * n in 1..64, S0 16-byte aligned; other arguments, errors and *status as for
+ * gdn_path_verify. */
+W12_API int gdn_wy_verify(const float* S0, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const float* alpha, const float* beta, const int32_t* parent, int64_t n, int64_t H,
+                          int64_t dk, int64_t dv, float* O, int32_t* status, void* stream);
+
 /* S[h] <- S[h] advanced by the accepted nodes path_nodes[1 .. *path_len] (device
  * values, as w12_lmhead_verify writes them: path_nodes[0] is the root), in
  * order; node inputs as for gdn_path_verify.  *path_len <= 0 commits nothing;

@@ -82,6 +82,7 @@ SIGNATURES = [
     ("w12_cert_head_argmax", ctypes.c_int, [_P, _I64, ctypes.POINTER(w12_i8_head), _MP, _P, _P, _P, _SZ, _P]),
     ("gdn_split3", ctypes.c_int, [_P, _I64, _P, _P, _P, _P]),
     ("gdn_path_verify", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
+    ("gdn_wy_verify", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
     ("gdn_commit", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P]),
 ]
 
@@ -468,6 +469,19 @@ def gdn_path_verify(S0, q, k, v, alpha, beta, parent, O=None, status=None, strea
     status = torch.zeros(1, dtype=torch.int32, device=S0.device) if status is None else _i32(status)
     _check(lib().gdn_path_verify(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(parent), n, H, dk,
                                  dv, _ptr(O), _ptr(status), _stream(stream)))
+    return O, status
+
+
+def gdn_wy_verify(S0, q, k, v, alpha, beta, parent, O=None, status=None, stream=None):
+    """gdn_path_verify's outputs in the WY form (every node once); dk 64 or 128, n <= 64."""
+    S0, alpha, beta = _f32(S0), _f32(alpha), _f32(beta)
+    q, k, v, parent = _bits16(q), _bits16(k), _bits16(v), _i32(parent)
+    H, dv, dk = S0.shape
+    n = parent.numel()
+    O = torch.empty((n, H, dv), dtype=torch.float32, device=S0.device) if O is None else _f32(O)
+    status = torch.zeros(1, dtype=torch.int32, device=S0.device) if status is None else _i32(status)
+    _check(lib().gdn_wy_verify(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(parent), n, H, dk,
+                               dv, _ptr(O), _ptr(status), _stream(stream)))
     return O, status
 
 

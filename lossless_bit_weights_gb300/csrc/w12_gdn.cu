@@ -410,6 +410,137 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_commit_reg(
   reg_store<DK>(S, base, dv - r0);
 }
 
+// ---- WY form: every node of the tree at once.  With gamma_t the product of alpha along
+// t's path, node t's state is S_t = gamma_t S0 + sum_{j on path(t)} (gamma_t/gamma_j) d_j k_j^T,
+// whose pseudo-values d_j solve, in node order (ancestors come first),
+//     d_t = beta_t (v_t - gamma_t S0 k_t - sum_{j ancestor of t} (gamma_t/gamma_j) (k_j.k_t) d_j),
+// and o_t = gamma_t S0 q_t + sum_{j on path(t)} (gamma_t/gamma_j) (k_j.q_t) d_j.  The state
+// enters only through S0 k_t and S0 q_t (all nodes in one pass over the state, rows in
+// registers); the rest is node-by-node scalars and a substitution per state row.  Rows are
+// independent, so a block takes (head, 32 rows).
+constexpr int kWyMaxNodes = 64;
+
+template <int DK>
+struct WyLayout {  // dynamic shared memory, in floats
+  static constexpr int P = 4 * (RegState<DK>::Q + 4);  // one padded vector
+  int n;
+  __device__ int kpad() const { return 0; }
+  __device__ int qpad() const { return n * P; }
+  __device__ int a() const { return 2 * n * P; }                       // S0 k_t, [n][32]
+  __device__ int b() const { return 2 * n * P + n * kRegRows; }        // S0 q_t
+  __device__ int d() const { return 2 * n * P + 2 * n * kRegRows; }    // pseudo-values
+  __device__ int vv() const { return 2 * n * P + 3 * n * kRegRows; }   // v of the block's rows
+  __device__ int kk() const { return 2 * n * P + 4 * n * kRegRows; }   // k_j.k_t, [n][n]
+  __device__ int kq() const { return kk() + n * n; }                   // k_j.q_t
+  __device__ int gam() const { return kq() + n * n; }
+  __device__ int bet() const { return gam() + n; }
+  __device__ int total() const { return bet() + n; }
+};
+
+size_t wy_smem(int64_t dk, int64_t n) {
+  const int64_t P = 4 * (dk / 4 + 4);
+  return (size_t)(2 * n * P + 4 * n * kRegRows + 2 * n * n + 2 * n) * 4 + (size_t)n * 4;
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kRegThreads) k_gdn_wy_verify(
+    const float* __restrict__ S0, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const uint16_t* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
+    const int32_t* __restrict__ parent, int64_t n64, int64_t H, int64_t dv, float* __restrict__ O,
+    int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) float wsm[];
+  __shared__ int32_t ok_sh;
+  const int n = (int)n64;
+  const WyLayout<DK> Lw{n};
+  int32_t* par = reinterpret_cast<int32_t*>(wsm + Lw.total());
+  const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kRegRows;
+  const int tid = threadIdx.x, p = tid & 3;
+  const int r = tid >> 2;
+  for (int t = tid; t < n; t += blockDim.x) par[t] = parent[t];
+  if (tid == 0) ok_sh = 1;
+  __syncthreads();
+  if (tid == 0) {
+    bool ok = par[0] == -1;
+    for (int t = 1; ok && t < n; ++t) ok = par[t] >= 0 && par[t] < t;
+    if (!ok) {
+      if (blockIdx.y == 0) atomicOr(status, 1);
+      ok_sh = 0;
+    } else {
+      float* g = wsm + Lw.gam();
+      g[0] = 1.f;  // the committed root: its update is already in S0
+      for (int t = 1; t < n; ++t) g[t] = alpha[(int64_t)t * H + h] * g[par[t]];
+    }
+  }
+  // node vectors (padded so the four quarters of k and q sit on distinct banks), v, beta
+  for (int e = tid; e < n * DK; e += blockDim.x) {
+    const int t = e / DK, c = e - t * DK;
+    wsm[Lw.kpad() + t * WyLayout<DK>::P + vpos<DK>(c)] = bf16v(k[((int64_t)t * H + h) * DK + c]);
+    wsm[Lw.qpad() + t * WyLayout<DK>::P + vpos<DK>(c)] = bf16v(q[((int64_t)t * H + h) * DK + c]);
+  }
+  for (int e = tid; e < n * kRegRows; e += blockDim.x) {
+    const int t = e / kRegRows, rr = e - t * kRegRows;
+    wsm[Lw.vv() + e] = r0 + rr < dv ? bf16v(v[((int64_t)t * H + h) * dv + r0 + rr]) : 0.f;
+  }
+  for (int t = tid; t < n; t += blockDim.x) wsm[Lw.bet() + t] = beta[(int64_t)t * H + h];
+  RegState<DK> S;
+  reg_load<DK>(S, S0 + (h * dv + r0) * DK, dv - r0);
+  __syncthreads();
+  if (!ok_sh) return;
+  // S0 k_t and S0 q_t of this block's rows, every node
+  for (int t = 0; t < n; ++t) {
+    const float at = reg_dot<DK>(S, wsm + Lw.kpad() + t * WyLayout<DK>::P);
+    const float bt = reg_dot<DK>(S, wsm + Lw.qpad() + t * WyLayout<DK>::P);
+    if (p == 0) {
+      wsm[Lw.a() + t * kRegRows + r] = at;
+      wsm[Lw.b() + t * kRegRows + r] = bt;
+    }
+  }
+  // (gamma_t/gamma_j) k_j.k_t and (gamma_t/gamma_j) k_j.q_t for j <= t (the four quarters
+  // of each padded vector, skipping the padding)
+  {
+    const float* gm = wsm + Lw.gam();
+    constexpr int Q = RegState<DK>::Q;
+    for (int e = tid; e < n * n; e += blockDim.x) {
+      const int t = e / n, j = e - t * n;
+      if (j > t) continue;
+      const float* kj = wsm + Lw.kpad() + j * WyLayout<DK>::P;
+      const float* kt = wsm + Lw.kpad() + t * WyLayout<DK>::P;
+      const float* qt = wsm + Lw.qpad() + t * WyLayout<DK>::P;
+      float g0 = 0.f, g1 = 0.f;
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        for (int m = 0; m < Q; ++m) {
+          const int c = qq * (Q + 4) + m;
+          g0 = fmaf(kj[c], kt[c], g0);
+          g1 = fmaf(kj[c], qt[c], g1);
+        }
+      const float ratio = gm[t] / gm[j];
+      wsm[Lw.kk() + t * n + j] = ratio * g0;
+      wsm[Lw.kq() + t * n + j] = ratio * g1;
+    }
+  }
+  __syncthreads();
+  // pseudo-values, node order, one thread per row
+  const float* gam = wsm + Lw.gam();
+  if (p == 0) {
+    float* d = wsm + Lw.d();
+    d[r] = 0.f;  // the root has no update here
+    for (int t = 1; t < n; ++t) {
+      float acc = wsm[Lw.vv() + t * kRegRows + r] - gam[t] * wsm[Lw.a() + t * kRegRows + r];
+      for (int j = par[t]; j > 0; j = par[j]) acc = fmaf(-wsm[Lw.kk() + t * n + j], d[j * kRegRows + r], acc);
+      d[t * kRegRows + r] = wsm[Lw.bet() + t] * acc;
+    }
+  }
+  __syncthreads();
+  // outputs: the four threads of a row split the nodes
+  const int64_t row = r0 + r;
+  for (int t = p; t < n; t += 4) {
+    float o = gam[t] * wsm[Lw.b() + t * kRegRows + r];
+    for (int j = t; j > 0; j = par[j]) o = fmaf(wsm[Lw.kq() + t * n + j], wsm[Lw.d() + j * kRegRows + r], o);
+    if (row < dv) O[((int64_t)t * H + h) * dv + row] = o;
+  }
+}
+
 // four threads per state row and a thread per element of k, whole warps
 int gdn_threads(int64_t dk, int64_t dv) {
   const int64_t t = 4 * dv > dk ? 4 * dv : dk;
@@ -482,6 +613,34 @@ int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* k, const
   if ((st = set_gdn_smem((const void*)k_gdn_path_verify, smem))) return st;
   k_gdn_path_verify<<<dim3((unsigned)n, (unsigned)H), gdn_threads(dk, dv), smem, (cudaStream_t)stream>>>(
       S0, q, k, v, alpha, beta, parent, n, H, dk, dv, O, status);
+  W12_LAUNCH_CHECK(fn);
+  return W12_OK;
+}
+
+int gdn_wy_verify(const float* S0, const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                  const float* beta, const int32_t* parent, int64_t n, int64_t H, int64_t dk, int64_t dv, float* O,
+                  int32_t* status, void* stream) {
+  const char* fn = "gdn_wy_verify";
+  int st = check_gdn_dims(H, dk, dv, fn);
+  if (st) return st;
+  if (dk != 64 && dk != 128) return fail(W12_ERR_SHAPE, "%s: dk=%lld (64 or 128)", fn, (long long)dk);
+  if (n < 1 || n > kWyMaxNodes)
+    return fail(W12_ERR_SHAPE, "%s: n=%lld out of range (1..%d)", fn, (long long)n, kWyMaxNodes);
+  if (dv > 65535 * (int64_t)kRegRows) return fail(W12_ERR_SHAPE, "%s: dv=%lld", fn, (long long)dv);
+  if (!S0 || !q || !k || !v || !alpha || !beta || !parent || !O || !status)
+    return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if ((((uintptr_t)S0) & 15u) != 0) return fail(W12_ERR_INVALID_ARG, "%s: S0 must be 16-byte aligned", fn);
+  const size_t smem = wy_smem(dk, n);
+  const dim3 grid((unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
+  if (dk == 128) {
+    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify<128>, smem))) return st;
+    k_gdn_wy_verify<128><<<grid, kRegThreads, smem, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
+                                                                           dv, O, status);
+  } else {
+    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify<64>, smem))) return st;
+    k_gdn_wy_verify<64><<<grid, kRegThreads, smem, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H, dv,
+                                                                          O, status);
+  }
   W12_LAUNCH_CHECK(fn);
   return W12_OK;
 }

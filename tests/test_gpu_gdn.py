@@ -155,3 +155,37 @@ def test_commit_after_acceptance(w12):
     O1, _ = w12.gdn_path_verify(S, dev(q[last:last + 1]), dev(k[:1]), dev(v[:1]), dev(alpha[:1]), dev(beta[:1]),
                                 dev(np.int32([-1])))
     assert_close(O1.cpu().numpy()[0], O.cpu().numpy()[last].astype(np.float64))
+
+
+@pytest.mark.parametrize("n,H,dk,dv,chain", [(1, 1, 64, 16, False), (5, 3, 64, 32, False), (32, 2, 128, 128, False),
+                                             (64, 2, 128, 100, False), (17, 1, 128, 1, True), (40, 2, 64, 200, False)])
+def test_wy_verify_matches_oracle(w12, n, H, dk, dv, chain):
+    rng = np.random.default_rng(n * 11 + dv)
+    S0, q, k, v, alpha, beta = inputs(rng, n, H, dk, dv)
+    parent = tree(rng, n, chain)
+    O, status = w12.gdn_wy_verify(dev(S0), dev(q), dev(k), dev(v), dev(alpha), dev(beta), dev(parent))
+    assert int(status.item()) == 0
+    assert_close(O.cpu().numpy(), oracle.gdn_tree(S0, q, k, v, alpha, beta, parent))
+
+
+def test_wy_verify_full_size_and_agrees_with_path_verify(w12):
+    rng = np.random.default_rng(47)
+    n, H, dk, dv = 32, 32, 128, 128
+    S0, q, k, v, alpha, beta = inputs(rng, n, H, dk, dv)
+    parent = tree(rng, n)
+    args = [dev(a) for a in (S0, q, k, v, alpha, beta, parent)]
+    O1, s1 = w12.gdn_wy_verify(*args)
+    O2, s2 = w12.gdn_path_verify(*args)
+    assert int(s1.item()) == 0 and int(s2.item()) == 0
+    ref = oracle.gdn_tree(S0, q, k, v, alpha, beta, parent)
+    assert_close(O1.cpu().numpy(), ref)
+    assert_close(O2.cpu().numpy(), ref)
+
+
+def test_wy_verify_flags_invalid_trees(w12):
+    rng = np.random.default_rng(48)
+    S0, q, k, v, alpha, beta = inputs(rng, 4, 1, 64, 16)
+    for bad in ([0, 0, 1, 2], [-1, 0, 2, 1], [-1, 0, 5, 1]):
+        _, status = w12.gdn_wy_verify(dev(S0), dev(q), dev(k), dev(v), dev(alpha), dev(beta),
+                                      dev(np.array(bad, np.int32)))
+        assert int(status.item()) & 1
