@@ -33,6 +33,14 @@
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *    device work is enqueued on it asynchronously; only w12_encode_plan
  *    synchronises it (it returns the escape count to the host).
+ *  - The GEMM kernels (w12_gemm*, the LM-head calls, w12_cert_head_argmax)
+ *    are launched with programmatic dependent launch: they may start while
+ *    the previous kernel on the stream finishes and begin reading the
+ *    matrix before it has completed; x, the workspace and the outputs are
+ *    touched only after it completes.  A kernel that signals early
+ *    (griddepcontrol.launch_dependents) must therefore not write the matrix
+ *    a following GEMM reads.  Kernels that do not signal, such as the
+ *    encoders here, complete before the GEMM starts.
  *  - bf16 tensors are passed as uint16_t bit patterns.
  *  - Shapes: 1 <= N, 1 <= K <= 65535 (the escape entry keeps the column in 16
  *    bits and reserves the all-ones column), 1 <= M.
