@@ -43,6 +43,8 @@ WORKLOAD = ("27B-class dense block: fused QKV 7168x5120, O 5120x5120, gate/up 34
             "down 5120x17408; W12 weights (per-channel N(0,s_c), s_c log-uniform [0.005,0.05], "
             "0.5% outliers x2^9, 0.2% zeros, 0.1% denormals); M=16 bf16 N(0,1) rows")
 HBM_FALLBACK = 6800.0
+# the same metric on both arms (the driver divides one by the other)
+METRIC = "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (34816x5120, M=16)
 # from an ncu capture of the current kernel; None when the kernel changed since.
 TRAFFIC_GATE_UP_M16 = 273613568 + 5381376
@@ -324,7 +326,7 @@ def run_reference(args, world, rank):
         total_w += n
     value = 2.0 * total_w / total_t / 1e9
     sample = f"{rows} channels of each block matrix per step (decode + fp64 GEMM at M={args.M})"
-    line = {"impl": "reference", "metric": "W12 verify-GEMM decoded-weight GB/s", "value": value, "unit": "GB/s",
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -509,7 +511,7 @@ def run_w12(args, world, rank, local):
 
     if rank == 0:
         line = {
-            "metric": "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)",
+            "metric": METRIC,
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
