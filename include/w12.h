@@ -93,8 +93,9 @@ typedef enum w12_status {
   W12_ERR_SHAPE = 2,            /* N, K or M out of range */
   W12_ERR_BUFFER_TOO_SMALL = 3, /* workspace smaller than the size query says */
   W12_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
-  W12_ERR_BOUNDS = 5,           /* device data inconsistent with the descriptor */
-  W12_ERR_TIMEOUT = 6           /* reserved: no call waits on the device */
+  W12_ERR_BOUNDS = 5,           /* device data inconsistent with the descriptor (w12_validate,
+                                   w12_workspace_status) */
+  W12_ERR_TIMEOUT = 6           /* a GEMM kernel's device-side wait ran out (w12_workspace_status) */
 } w12_status;
 
 /* A W12 matrix in device memory (layout above).  The struct itself lives in
@@ -155,9 +156,10 @@ W12_API int w12_export_canonical(const w12_matrix* A, uint8_t* hi_out, uint8_t* 
 /* ---- verify GEMM (pages: "What's different", decode-fused stream-K GEMM) -- */
 
 /* Workspace bytes for w12_gemm / w12_gemm_q8 with these shapes on the current
- * device.  The workspace's first w12_gemm_counter_bytes(N) bytes are tile
- * counters that must be zero before the first call; every completed call
- * leaves them zero again (re-zero after a failed call). */
+ * device.  The workspace's first w12_gemm_counter_bytes(N) bytes (an error word
+ * in the first 256 bytes, then one tile counter per row block) must be zero
+ * before the first call; every call that completes without a device error
+ * leaves them zero again, and w12_workspace_status clears them after one. */
 W12_API size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 W12_API size_t w12_gemm_counter_bytes(int64_t N);
 
@@ -172,6 +174,39 @@ W12_API int w12_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y
 W12_API int w12_gemm_q8(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* ---- device errors of the GEMM kernels -------------------------------------
+ * Every wait of a GEMM kernel (for records to land, a buffer to be released, an
+ * accumulator to be ready) is bounded.  A CTA whose wait runs out stops its work,
+ * waits for its own copies and MMAs in flight, frees its tensor memory and sets
+ * a bit in the workspace's error word; the launch then ends normally and the call
+ * returned W12_OK, but its outputs are incomplete.  A CTA that meets an escape
+ * offset beyond the matrix's escape list clamps it and sets another bit.  The
+ * word covers w12_gemm, w12_gemm_q8, the LM-head calls and w12_cert_head_argmax
+ * (whose workspaces start with the GEMM's). */
+
+/* Synchronises `stream`, then stores in *status (host) W12_ERR_TIMEOUT if a wait
+ * of a call on this workspace ran out since the last query, else W12_ERR_BOUNDS if
+ * an escape offset was out of range, else W12_OK.  After an error it zeroes the
+ * whole workspace (ws_bytes), so that tile counters left raised by a CTA that gave
+ * up do not disturb the next call.  Returns W12_OK, or W12_ERR_INVALID_ARG /
+ * W12_ERR_BUFFER_TOO_SMALL (ws_bytes < 256) / W12_ERR_CUDA. */
+W12_API int w12_workspace_status(void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/* Diagnostic for tests of the path above: bounds the GEMM kernels' waits for another
+ * warp's work at `cycles` SM clock cycles on the current device (cycles <= 0
+ * restores the default, 2^31, about a second).  Waits for a CTA's own copies and
+ * MMAs keep the default.  Synchronous; kernels launched after it returns see it. */
+W12_API int w12_set_wait_limit(int64_t cycles);
+
+/* Checks the index arrays of A against its descriptor without touching the planes
+ * (the GEMM trusts them): esc_tile_ptr rises from 0 to n_esc; every entry of a
+ * tile's run is an even slot of the 32x64 tile image, names a channel < N and a
+ * column < K, and follows the previous entry of the tile in (channel, column)
+ * order; every window base is in 1..239.  Writes W12_OK or W12_ERR_BOUNDS to
+ * *status (device int32).  Reads esc only at offsets below n_esc.  Asynchronous.
+ * Errors: W12_ERR_INVALID_ARG, W12_ERR_SHAPE. */
+W12_API int w12_validate(const w12_matrix* A, int32_t* status, void* stream);
+
 /* ---- verify GEMM without a caller workspace ------------------------------
  * Not part of the method: the pages have no counterpart.  It is w12_gemm for
  * callers that cannot give the library a workspace: an engine whose memory
@@ -183,7 +218,8 @@ W12_API int w12_gemm_q8(const uint16_t* x, int64_t M, const w12_matrix* A, float
  *    exits.  Nothing is allocated per call.
  *  - The first call on a device looks up the array's device address with that
  *    device current.  Make that first call before any stream capture.
- *  - Each call clears the array's counters on `stream` before the GEMM.
+ *  - Each call clears the array's error word and counters on `stream` before the
+ *    GEMM; a call refused by an argument check touches nothing.
  *  - All calls share the one array: calls that can overlap on the GPU (other
  *    streams, other host threads on the same device) race and corrupt each
  *    other's results.  Serialise them.

@@ -64,6 +64,9 @@ SIGNATURES = [
     ("w12_gemm_counter_bytes", _SZ, [_I64]),
     ("w12_gemm", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
     ("w12_gemm_q8", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
+    ("w12_workspace_status", ctypes.c_int, [_P, _SZ, ctypes.POINTER(_I32), _P]),
+    ("w12_set_wait_limit", ctypes.c_int, [_I64]),
+    ("w12_validate", ctypes.c_int, [_MP, _P, _P]),
     ("w12_gemm_noalloc_max_scratch", _SZ, []),
     ("w12_gemm_noalloc", ctypes.c_int, [_P, _I64, _MP, _P, _P]),
     ("w12_lmhead_workspace_size", _SZ, [_I64, _I64, _I64]),
@@ -231,6 +234,33 @@ class Workspace:
         if nbytes > self.buf.numel():
             self.buf = torch.zeros(int(nbytes), dtype=torch.uint8, device=self.device)
         return self.buf
+
+    def status(self, stream=None) -> int:
+        """w12_workspace_status: W12_OK, W12_ERR_TIMEOUT or W12_ERR_BOUNDS for the calls made
+        on this workspace since the last query (synchronises the stream; clears the
+        workspace after an error)."""
+        st = ctypes.c_int32(-1)
+        _check(lib().w12_workspace_status(_ptr(self.buf), self.buf.numel(), ctypes.byref(st), _stream(stream)))
+        return int(st.value)
+
+    def check(self, stream=None) -> None:
+        """Raises W12Error if a GEMM call on this workspace met a device error."""
+        st = self.status(stream)
+        if st != W12_OK:
+            raise W12Error(st, "a GEMM kernel reported a device error on this workspace")
+
+
+def w12_set_wait_limit(cycles: int) -> None:
+    """Diagnostic: bound of the GEMM kernels' waits for another warp (0 = default)."""
+    _check(lib().w12_set_wait_limit(int(cycles)))
+
+
+def w12_validate(A: "W12Matrix", status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Checks A's escape index and window bases on the device; returns a device int32
+    tensor holding W12_OK or W12_ERR_BOUNDS."""
+    status = torch.empty(1, dtype=torch.int32, device=A.device) if status is None else _i32(status)
+    _check(lib().w12_validate(A.desc(), _ptr(status), _stream(stream)))
+    return status
 
 
 def gemm_workspace_size(M: int, N: int, K: int) -> int:

@@ -6,6 +6,7 @@
 // everything else (out-of-window, zeros, denormals) exact in a per-channel
 // escape list.  The device layout (tiles of 32 channels x 64 columns) is the
 // one include/w12.h documents.
+#include <algorithm>
 #include <cstdint>
 
 #include "w12_internal.cuh"
@@ -347,6 +348,43 @@ __global__ void __launch_bounds__(256) k_export_esc(const uint32_t* __restrict__
   if (pass == 0 && n < N) rowptr[n] = cnt;
 }
 
+// ---------------------------------------------------------------- index validation
+
+// One thread per tile, then one per channel.  A tile's escape offsets must rise, start at
+// 0 and end at n_esc; each entry must lie within the list, name an even byte slot of the
+// 32x64 tile image, a real weight (channel < N, column < K), and come after the previous
+// entry of its tile in (channel, column) order.  Every window base must be in 1..239.  Any
+// violation sets *status to W12_ERR_BOUNDS; only offsets within 0..n_esc are dereferenced.
+__global__ void __launch_bounds__(256) k_validate(const uint32_t* __restrict__ tile_ptr, const uint32_t* __restrict__ esc,
+                                                  const uint8_t* __restrict__ base, int64_t N, int64_t K, int64_t KC,
+                                                  int64_t T, uint32_t n_esc, int32_t* __restrict__ status) {
+  bool bad = false;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t e0 = tile_ptr[t], e1 = tile_ptr[t + 1];
+    if ((t == 0 && e0 != 0u) || (t == T - 1 && e1 != n_esc) || e1 < e0 || e1 > n_esc) {
+      bad = true;
+      continue;
+    }
+    int64_t rt, kc;
+    tile_coords(t, KC, rt, kc);
+    int prev = -1;
+    for (uint32_t e = e0; e < e1; ++e) {
+      const uint32_t ent = esc[e], slot = esc_slot(ent);
+      const int rr = esc_row(ent), kk = esc_col(ent), key = rr * kTileK + kk;
+      if ((slot & 1u) || slot >= 4096u || rt * kTileRows + rr >= N || kc * kTileK + kk >= K || key <= prev) {
+        bad = true;
+        break;
+      }
+      prev = key;
+    }
+  }
+  for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t b = base[n];
+    if (b < 1u || b > 239u) bad = true;
+  }
+  if (bad) *status = W12_ERR_BOUNDS;
+}
+
 inline unsigned blocks_for(int64_t warps) { return (unsigned)((warps + 7) / 8); }
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -436,6 +474,21 @@ int w12_export_canonical(const w12_matrix* A, uint8_t* hi_out, uint8_t* lo_out, 
     k_export_esc<<<blocks_for(RT), 256, 0, s>>>(A->esc_tile_ptr, A->esc, A->N, RT, KC, 1, rowptr_out, esc_out);
     W12_LAUNCH_CHECK("w12_export_canonical: fill");
   }
+  return W12_OK;
+}
+
+int w12_validate(const w12_matrix* A, int32_t* status, void* stream) {
+  const char* fn = "w12_validate";
+  int st = check_matrix(A, false, fn);
+  if (st) return st;
+  if (!status) return fail(W12_ERR_INVALID_ARG, "%s: null status", fn);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t KC = k_chunks(A->K), T = row_tiles(A->N) * KC;
+  W12_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s));
+  const int64_t work = T > A->N ? T : A->N;
+  const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 4096);
+  k_validate<<<blocks, 256, 0, s>>>(A->esc_tile_ptr, A->esc, A->base, A->N, A->K, KC, T, (uint32_t)A->n_esc, status);
+  W12_LAUNCH_CHECK(fn);
   return W12_OK;
 }
 

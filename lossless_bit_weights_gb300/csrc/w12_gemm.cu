@@ -42,6 +42,17 @@ namespace {
 constexpr int kEscRun = 128;  // escape entries a record stage holds
 constexpr int kMinIters = 4;  // fewest units per CTA
 
+// Bits of the workspace's error word (its first 4 bytes), set by a CTA that gave up or
+// met a bad escape index, read and cleared by w12_workspace_status.
+constexpr uint32_t kErrTimeout = 1u;  // a wait for another warp's work ran out
+constexpr uint32_t kErrBounds = 2u;   // an escape offset lay outside the escape list
+
+// Bound of the kernel's waits for another warp's work (records landed, a stage or buffer
+// released, an accumulator ready), in SM clock cycles.  w12_set_wait_limit lowers it to
+// exercise the timeout path.  Waits for a warp's own copies and MMAs in flight keep the
+// default bound, so a CTA that gives up still leaves with nothing in flight.
+__constant__ long long c_wait_limit = kWaitCycles;
+
 // EPI_I8: the weights are INT8 codes (sign<<7 | |q|, in the hi-plane layout; no lo plane,
 // window bases or escapes) and the output is scale[n] * acc.
 enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_I8 = 2 };
@@ -67,6 +78,7 @@ struct GemmArgs {
   // measured 6% slower (only the offsets of the members after it changed).
   int64_t RB;  // row blocks of the matrix
   const float* scale;  // EPI_I8: per-channel scale
+  uint32_t n_esc;      // escape entries; escape offsets are clamped to it
 };
 
 __device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
@@ -235,9 +247,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Wait for another warp's work on a barrier phase, bounded by c_wait_limit.
+__device__ __forceinline__ bool peer_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_bounded(bar, parity, c_wait_limit);
+}
+
 // Bounded barrier wait whose outcome is the same in every lane of the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity));
+  return __all_sync(0xFFFFFFFFu, peer_wait(bar, parity));
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
@@ -253,7 +270,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target) {
     const long long start = clock64();
     while (*reinterpret_cast<const volatile uint32_t*>(c) < target) {
       __nanosleep(64);
-      if (clock64() - start > (1ll << 31)) {
+      if (clock64() - start > c_wait_limit) {
         ok = false;
         break;
       }
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   tc_fence_after();
   const uint32_t tmem0 = misc0[0];  // kept in a register: the teardown frees exactly this
   const uint32_t tmem = tmem0 + (uint32_t)(pipe * P::kTmemCols);
-  bool bail = false;
+  bool bail = false, bad_index = false;
 
   if (!active) {
     // a pipeline with no place in the partition goes straight to the teardown
@@ -441,7 +458,13 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, w0, src & 31);
         const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, w1, src & 31);
         const uint32_t tpv = src < 32 ? v0 : v1;
-        const uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
+        uint32_t t_first = __shfl_sync(0xFFFFFFFFu, tpv, 0), t_last = __shfl_sync(0xFFFFFFFFu, tpv, 4);
+        // offsets past the escape list (a damaged index) are clamped and reported
+        if (t_last > a.n_esc || t_first > t_last) {
+          bad_index = true;
+          t_last = min(t_last, a.n_esc);
+          t_first = min(t_first, t_last);
+        }
         e0 = t_first & ~3u;
         uint32_t e1 = (t_last + 3u) & ~3u;
         if (e1 > e0 + kEscRun) e1 = e0 + kEscRun;
@@ -496,7 +519,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       int issued = 0;
       for (int j = 0; j < nun; ++j) {
         const int s = j % SX;
-        if (j >= SX && !mbar_wait_bounded(x_empty0 + 8 * s, (uint32_t)(((j / SX) - 1) & 1))) {
+        if (j >= SX && !peer_wait(x_empty0 + 8 * s, (uint32_t)(((j / SX) - 1) & 1))) {
           bail = true;
           break;
         }
@@ -524,11 +547,11 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       uint32_t xph = 0, aph = 0;
       for (int j = 0; j < nunp; ++j) {
         const bool first = (j == 0) || (kc == 0);
-        if (first && j > 0 && !mbar_wait_bounded(acc_empty, (uint32_t)((seg - 1) & 1))) {
+        if (first && j > 0 && !peer_wait(acc_empty, (uint32_t)((seg - 1) & 1))) {
           bail = true;
           break;
         }
-        if (!mbar_wait_bounded(a_full0 + 8 * gi, aph) || !mbar_wait_bounded(x_full0 + 8 * s, xph)) {
+        if (!peer_wait(a_full0 + 8 * gi, aph) || !peer_wait(x_full0 + 8 * s, xph)) {
           bail = true;
           break;
         }
@@ -555,7 +578,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       }
       // a wide pipeline past its last row block still frees the shared x stages it skips
       for (int j = nunp; j < nun && !bail; ++j) {
-        if (!mbar_wait_bounded(x_full0 + 8 * s, xph)) {
+        if (!peer_wait(x_full0 + 8 * s, xph)) {
           bail = true;
           break;
         }
@@ -626,7 +649,9 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         }
         // this row tile's escapes: entry ta + lane into a register (the rare tail past 32 stays in memory)
         const uint32_t* hdr = reinterpret_cast<const uint32_t*>(rec + P::kOffHdr);
-        const uint32_t ta = I8 ? 0u : hdr[tl], tb = I8 ? 0u : hdr[tl + 1], e0 = I8 ? 0u : hdr[5];
+        // the tile's escape range, clamped to the escape list (the producer reports a bad index)
+        const uint32_t tb = I8 ? 0u : min(hdr[tl + 1], a.n_esc), ta = I8 ? 0u : min(hdr[tl], tb);
+        const uint32_t e0 = I8 ? 0u : hdr[5];
         const uint32_t cnt = tb - ta;
         uint32_t ent = 0u;
         if ((uint32_t)lane < cnt) {
@@ -654,11 +679,13 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           *reinterpret_cast<uint4*>(row + (((2 * t + 1) ^ g) << 4)) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
         }
         __syncwarp();  // the decoded stores of all lanes land before any escape overwrites a slot
-        if ((uint32_t)lane < cnt) *reinterpret_cast<uint16_t*>(atp + esc_slot(ent)) = (uint16_t)esc_raw(ent);
+        // a slot is an even byte offset below 4096 (32 rows of 128 bytes): the mask keeps a
+        // damaged entry inside this warp's tile
+        if ((uint32_t)lane < cnt) *reinterpret_cast<uint16_t*>(atp + (esc_slot(ent) & 0xFFEu)) = (uint16_t)esc_raw(ent);
         if (cnt > 32u) {
           for (uint32_t e = ta + 32 + lane; e < tb; e += 32) {
             const uint32_t en = __ldg(a.esc + e);
-            *reinterpret_cast<uint16_t*>(atp + esc_slot(en)) = (uint16_t)esc_raw(en);
+            *reinterpret_cast<uint16_t*>(atp + (esc_slot(en) & 0xFFEu)) = (uint16_t)esc_raw(en);
           }
         }
         fence_proxy_async_smem();  // this thread's generic-proxy stores -> tensor-core reads
@@ -769,7 +796,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   }
 
   // ---- teardown: every warp reaches this point, TMEM is always freed
-  if (bail && lane == 0) atomicOr(a.error, 1u);
+  if (lane == 0 && (bail || bad_index)) atomicOr(a.error, (bail ? kErrTimeout : 0u) | (bad_index ? kErrBounds : 0u));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -859,8 +886,10 @@ int64_t partition_ctas(int64_t T, int sms, int bpsm) {
 
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// Workspace: the error word (first 256 bytes), the tile counters, then scratch that every
+// call writes before reading.  The error word and counters start at zero.
 struct WsLayout {
-  size_t counters, error, slots, xpad, pbest, total;
+  size_t error, counters, slots, xpad, pbest, total;
 };
 
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
@@ -870,10 +899,9 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   const int64_t G = partition_ctas(TP, sms, ls.parts);
   const int64_t n_slots = ls.mode == kModePair ? 2 * ((RB + 1) / 2 + G) : RB + G;
   WsLayout L{};
-  L.counters = 0;
-  size_t off = align256((size_t)RB * 4);
-  L.error = off;
-  off += 256;
+  L.error = 0;
+  L.counters = 256;
+  size_t off = 256 + align256((size_t)RB * 4);
   L.slots = off;  // one slot of 128 channels x nt tokens per (partition part, row block) pair
   off = align256(off + (size_t)n_slots * (size_t)(kBlockTiles * kTileRows) * (size_t)ls.nt * 4);
   L.xpad = off;
@@ -952,25 +980,35 @@ int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, 
   }
 }
 
-int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_t* tok, bool q8, bool argmax,
-             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn, const float* i8_scale = nullptr) {
-  // i8_scale: A->hi holds INT8 codes (the caller has checked A's shape and pointers)
-  int st = i8_scale ? W12_OK : check_matrix(A, !q8, fn);
+// Host-side checks of a GEMM call's arguments (everything but the workspace); a call that
+// fails them touches no memory.
+int check_gemm_args(const uint16_t* x, int64_t M, const w12_matrix* A, const float* y, const int32_t* tok, bool q8,
+                    bool argmax, bool i8, const char* fn) {
+  // i8: A->hi holds INT8 codes (the caller has checked A's shape and pointers)
+  int st = i8 ? W12_OK : check_matrix(A, !q8, fn);
   if (st) return st;
   if (!x || (!argmax && !y) || (argmax && !tok)) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
-  if (!ws) return fail(W12_ERR_INVALID_ARG, "%s: null workspace", fn);
   if ((((uintptr_t)A->hi | (uintptr_t)A->lo | (uintptr_t)A->esc) & 15u) != 0)
     return fail(W12_ERR_INVALID_ARG, "%s: hi, lo and esc must be 16-byte aligned", fn);
+  const int64_t T = row_blocks(A->N) * k_chunks(A->K);
+  if (T >= (int64_t(1) << 30))
+    return fail(W12_ERR_SHAPE, "%s: %lld row blocks x %lld column chunks exceed 2^30 units", fn,
+                (long long)row_blocks(A->N), (long long)k_chunks(A->K));
+  return W12_OK;
+}
+
+int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_t* tok, bool q8, bool argmax,
+             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn, const float* i8_scale = nullptr) {
+  int st = check_gemm_args(x, M, A, y, tok, q8, argmax, i8_scale != nullptr, fn);
+  if (st) return st;
+  if (!ws) return fail(W12_ERR_INVALID_ARG, "%s: null workspace", fn);
   int sms = 0;
   if ((st = device_sms(&sms))) return st;
   const WsLayout L = ws_layout(M, A->N, A->K, argmax, sms);
   if (ws_bytes < L.total)
     return fail(W12_ERR_BUFFER_TOO_SMALL, "%s: workspace %zu bytes < %zu required", fn, ws_bytes, L.total);
-  const int64_t RB = row_blocks(A->N), RT = row_tiles(A->N), KC = k_chunks(A->K), T = RB * KC;
-  if (T >= (int64_t(1) << 30))
-    return fail(W12_ERR_SHAPE, "%s: %lld row blocks x %lld column chunks exceed 2^30 units", fn, (long long)RB,
-                (long long)KC);
+  const int64_t RB = row_blocks(A->N), RT = row_tiles(A->N), KC = k_chunks(A->K);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
   // x through a tensor map needs a 16-byte aligned base and a row pitch that is a multiple of 16 bytes
@@ -1006,6 +1044,7 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.ldp = M;
   a.mul = W12_DECODE_MUL;
   a.scale = i8_scale;
+  a.n_esc = i8_scale ? 0u : (uint32_t)A->n_esc;
   CUtensorMap map;
   if ((st = make_x_map(&map, xs, M, A->K, ldx, ls.nt))) return st;
   for (int64_t m0 = 0; m0 < M; m0 += ls.nt) {
@@ -1061,7 +1100,7 @@ using namespace w12;
 
 extern "C" {
 
-size_t w12_gemm_counter_bytes(int64_t N) { return N >= 1 ? align256((size_t)row_blocks(N) * 4) : 0; }
+size_t w12_gemm_counter_bytes(int64_t N) { return N >= 1 ? 256 + align256((size_t)row_blocks(N) * 4) : 0; }
 
 size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || N < 1 || K < 1 || K > kMaxK) return 0;
@@ -1092,6 +1131,26 @@ int w12_lmhead_argmax(const uint16_t* x, int64_t M, const w12_matrix* head, int3
 int w12_lmhead_argmax_q8(const uint16_t* x, int64_t M, const w12_matrix* head, int32_t* tok, void* ws,
                          size_t ws_bytes, void* stream) {
   return run_gemm(x, M, head, nullptr, tok, true, true, ws, ws_bytes, (cudaStream_t)stream, "w12_lmhead_argmax_q8");
+}
+
+int w12_workspace_status(void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+  const char* fn = "w12_workspace_status";
+  if (!ws || !status) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (ws_bytes < 256) return fail(W12_ERR_BUFFER_TOO_SMALL, "%s: a workspace holds at least 256 bytes", fn);
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t word = 0;
+  W12_CUDA_TRY(cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s));
+  W12_CUDA_TRY(cudaStreamSynchronize(s));
+  *status = (word & kErrTimeout) ? W12_ERR_TIMEOUT : (word & kErrBounds) ? W12_ERR_BOUNDS : W12_OK;
+  // a CTA that gave up may have left tile counters raised: start the next call clean
+  if (word) W12_CUDA_TRY(cudaMemsetAsync(ws, 0, ws_bytes, s));
+  return W12_OK;
+}
+
+int w12_set_wait_limit(int64_t cycles) {
+  const long long v = cycles > 0 ? (long long)cycles : kWaitCycles;
+  W12_CUDA_TRY(cudaMemcpyToSymbol(c_wait_limit, &v, sizeof(v)));
+  return W12_OK;
 }
 
 }  // extern "C"
@@ -1141,9 +1200,9 @@ size_t w12_gemm_noalloc_max_scratch(void) { return w12::kFixedScratchBytes; }
 int w12_gemm_noalloc(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, void* stream) {
   using namespace w12;
   const char* fn = "w12_gemm_noalloc";
-  int st = check_matrix(A, true, fn);
+  // every argument check comes before the scratch is touched: a refused call leaves it alone
+  int st = check_gemm_args(x, M, A, y, nullptr, false, false, false, fn);
   if (st) return st;
-  if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
   int sms = 0;
   if ((st = device_sms(&sms))) return st;
   const WsLayout L = ws_layout(M, A->N, A->K, false, sms);
@@ -1155,7 +1214,7 @@ int w12_gemm_noalloc(const uint16_t* x, int64_t M, const w12_matrix* A, float* y
   void* scratch = nullptr;
   if ((st = fixed_scratch_address(&scratch))) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  // the tile counters and the error word must start at zero on every call
+  // the error word and the tile counters must start at zero on every call
   W12_CUDA_TRY(cudaMemsetAsync(scratch, 0, L.slots, s));
   return run_gemm(x, M, A, y, nullptr, false, false, scratch, kFixedScratchBytes, s, fn);
 }

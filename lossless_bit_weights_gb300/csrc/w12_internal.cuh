@@ -238,22 +238,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Default bound of every device-side wait, in SM clock cycles: about a second.
+constexpr long long kWaitCycles = 1ll << 31;
+
 // Slow path of mbar_wait_bounded: try_wait (the thread may be suspended in
-// hardware until the phase completes) up to a clock limit of about 2^31
-// cycles (~1 s).  Returns false when the limit ran out.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
+// hardware until the phase completes) until `limit` clock cycles have passed.
+// Returns false when the limit ran out.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, long long limit) {
   const long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > (1ll << 31)) return false;
+    if (clock64() - start > limit) return false;
   }
   return true;
 }
 
 // Waits for the barrier phase with parity `parity`, bounded; one non-blocking
 // test first, so a phase that has already completed costs two instructions.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit = kWaitCycles) {
   if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity);
+  return mbar_wait_slow(bar, parity, limit);
 }
 
 // Global -> shared bulk copy completing on an mbarrier (size multiple of 16, both addresses 16-byte aligned).

@@ -86,3 +86,26 @@ def test_certified_head_and_recurrent_argument_errors():
     assert lib.gdn_path_verify(p, p, p, p, p, p, None, 4, 2, 128, 128, p, p, None) == 1
     assert lib.gdn_commit(p, p, p, p, p, p, p, 0, 2, 128, 128, p, None) == 2
     assert lib.gdn_commit(p, p, p, p, p, None, p, 4, 2, 128, 128, p, None) == 1
+
+
+def test_error_queries_and_noalloc_check_arguments_before_any_cuda_call():
+    """w12_workspace_status, w12_validate and w12_gemm_noalloc refuse bad arguments on the
+    host: on a machine without a GPU the answer is the argument error, not a CUDA error,
+    so no device work (and for w12_gemm_noalloc no clearing of its scratch) came first."""
+    import ctypes
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    st = ctypes.c_int32(-1)
+    p = ctypes.c_void_p(256)
+    assert lib.w12_workspace_status(None, 4096, ctypes.byref(st), None) == 1
+    assert lib.w12_workspace_status(p, 4096, None, None) == 1
+    assert lib.w12_workspace_status(p, 128, ctypes.byref(st), None) == 3
+    A = w12.w12_matrix(64, 64, 256, 256, 256, 256, 256, 4)
+    assert lib.w12_validate(ctypes.byref(A), None, None) == 1
+    assert lib.w12_validate(None, p, None) == 1
+    assert lib.w12_gemm_noalloc(None, 4, ctypes.byref(A), p, None) == 1
+    mis = w12.w12_matrix(64, 64, 264, 256, 256, 256, 256, 4)
+    assert lib.w12_gemm_noalloc(p, 4, ctypes.byref(mis), p, None) == 1
+    assert b"aligned" in lib.w12_last_error()
+    assert lib.w12_gemm_noalloc(p, 0, ctypes.byref(A), p, None) == 2
+    assert lib.w12_gemm_counter_bytes(5120) == 256 + 256       # error word, then 40 counters

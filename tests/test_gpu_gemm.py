@@ -80,10 +80,12 @@ def test_deterministic_repeats(w12):
         assert torch.equal(w12.w12_gemm_q8(x, A, ws=ws), refq)
 
 
-@pytest.mark.parametrize("M", [100, 256])
+@pytest.mark.parametrize("M", [32, 100, 192, 256])
 def test_deterministic_repeats_wide(w12, M):
-    """Back-to-back launches at 64..256 tokens (row-block pairs, shallow record rings):
-    every launch gives the same bits, and a sample of channels matches the oracle."""
+    """Back-to-back launches on a full-size gate/up matrix at 32 tokens (two pipelines per
+    CTA), 100 (row-block pairs), 192 and 256 (one pipeline, shallow record rings): every
+    launch gives the same bits (the stream-K sums run in a fixed order), and a sample of
+    channels matches the oracle."""
     N, K = 34816, 5120
     W = device_weights(0, 0, 2, N, K)
     A = w12.encode(W)
@@ -136,5 +138,62 @@ def test_block_m32_q8_sampled(w12):
     sampled_block_check(w12, layer=63, M=32, q8=True)
 
 
+def test_block_m32_exact_sampled(w12):
+    """The exact pass of the 64-layer stack at 32 tokens: all four full-size block
+    matrices of one layer, in the launch configuration the stack uses."""
+    sampled_block_check(w12, layer=5, M=32, q8=False)
+
+
 def test_block_m192_sampled(w12):
     sampled_block_check(w12, layer=1, M=192, q8=False, n_rows=24)
+
+
+def escape_dense_matrix(N, K, seed):
+    """Weights of the usual recipe with escapes planted far above its rate: the first
+    32x64 tile holds nothing but escapes (zeros of both signs, denormals, values 2^20
+    above or 2^40 below the window), the next row tile's second chunk 8% escapes and
+    the third row tile's third chunk 25%, so a row tile exceeds 32 escapes and a 128x64
+    unit exceeds 128 (the escape list of a unit is then read partly from global memory).
+    Every value stays finite."""
+    W = synth.weights(0, 77, seed, N, K).copy()
+    rng = np.random.default_rng(seed)
+
+    def plant(rows, cols, frac):
+        blk = W[rows, cols]
+        pick = rng.random(blk.shape) < frac
+        kind = rng.integers(0, 4, blk.shape)
+        sign = (rng.integers(0, 2, blk.shape) << 15).astype(np.uint16)
+        e = (blk >> 7) & 0xFF
+        den = sign | rng.integers(1, 128, blk.shape).astype(np.uint16)
+        up = np.where(e + 20 <= 254, (blk & 0x807F) | ((e + 20) << 7), blk).astype(np.uint16)
+        dn = np.where(e >= 41, (blk & 0x807F) | ((e - 40) << 7), den).astype(np.uint16)
+        new = np.choose(kind, [sign, den, up, dn]).astype(np.uint16)
+        W[rows, cols] = np.where(pick, new, blk)
+
+    plant(slice(0, 32), slice(0, 64), 1.0)
+    plant(slice(32, 64), slice(64, 128), 0.08)
+    plant(slice(64, 96), slice(128, 192), 0.25)
+    return W
+
+
+@pytest.mark.parametrize("M", [5, 16, 40, 192])
+@pytest.mark.parametrize("q8", [False, True])
+def test_escape_dense(w12, M, q8):
+    """Escapes restored exactly, also where a tile or unit holds more than its stage keeps:
+    the GEMM against the oracle, the codec bit-exact."""
+    N, K = 300, 700
+    W = escape_dense_matrix(N, K, 3)
+    enc = oracle.encode(W)
+    cols = enc.esc >> 16
+    first_tile = sum(int((cols[enc.rowptr[r]:enc.rowptr[r + 1]] < 64).sum()) for r in range(32))
+    assert first_tile == 2048          # the first tile is all escapes
+    A = w12.encode(to_dev16(W))
+    assert A.n_esc == enc.n_esc and enc.n_esc > 2048 + 200
+    assert np.array_equal(to_np16(w12.w12_decode(A)), W)
+    x = synth.activations(1, 77, M, M, K)
+    Wq = oracle.decode_q8(enc) if q8 else oracle.decode(enc)
+    y64, B = oracle.gemm(x, Wq)
+    ws = w12.Workspace()
+    y = (w12.w12_gemm_q8 if q8 else w12.w12_gemm)(to_dev16(x), A, ws=ws).cpu().numpy()
+    assert_gemm_close(y, y64, B, REL)
+    assert ws.status() == 0
