@@ -410,135 +410,310 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_commit_reg(
   reg_store<DK>(S, base, dv - r0);
 }
 
-// ---- WY form: every node of the tree at once.  With gamma_t the product of alpha along
-// t's path, node t's state is S_t = gamma_t S0 + sum_{j on path(t)} (gamma_t/gamma_j) d_j k_j^T,
+// ---- WY form on the tensor core: every node of the tree at once.  With gamma_t the
+// product of alpha along t's path, node t's state is
+//     S_t = gamma_t S0 + sum_{j on path(t)} (gamma_t/gamma_j) d_j k_j^T,
 // whose pseudo-values d_j solve, in node order (ancestors come first),
 //     d_t = beta_t (v_t - gamma_t S0 k_t - sum_{j ancestor of t} (gamma_t/gamma_j) (k_j.k_t) d_j),
 // and o_t = gamma_t S0 q_t + sum_{j on path(t)} (gamma_t/gamma_j) (k_j.q_t) d_j.  The state
-// enters only through S0 k_t and S0 q_t (all nodes in one pass over the state, rows in
-// registers); the rest is node-by-node scalars and a substitution per state row.  Rows are
-// independent, so a block takes (head, 32 rows).
+// enters only through the products S0 [k_0 .. k_{n-1} q_0 .. q_{n-1}], one matrix product
+// per head.  It runs on the tensor core in bf16 with the float state held exactly as three
+// bf16 pieces, S0 = s1 + s2 + s3 (gdn_split3's split): the pieces are the A operand (128
+// state rows x 3 dk columns), the node vectors the B operand (each repeated for the three
+// pieces), so every product of a piece and a k or q element is exact and the tensor core
+// accumulates them in fp32.  A second product gives the node tables k_t.k_j and q_t.k_j.
+// The per-row substitution over the tree then runs on the CUDA cores, one thread per row.
+//
+// One CTA per (head, 128 state rows): the rows arrive by one bulk copy, 16 warps split them
+// into the three pieces in the operands' 128-byte-swizzled layout, one thread issues the
+// MMAs (accumulators in tensor memory), four warps read the state products back (lane =
+// state row) and four the node tables, four warps run the substitution and all sixteen
+// the outputs.
 constexpr int kWyMaxNodes = 64;
+constexpr int kWyRows = 128;                 // state rows per CTA: the MMA's M
+constexpr int kWyThreads = 512;
+constexpr int kWyTile = kWyRows * 128;       // one operand tile: 128 rows x 64 bf16 (16 KB)
 
 template <int DK>
-struct WyLayout {  // dynamic shared memory, in floats
-  static constexpr int P = 4 * (RegState<DK>::Q + 4);  // one padded vector
-  int n;
-  __device__ int kpad() const { return 0; }
-  __device__ int qpad() const { return n * P; }
-  __device__ int a() const { return 2 * n * P; }                       // S0 k_t, [n][32]
-  __device__ int b() const { return 2 * n * P + n * kRegRows; }        // S0 q_t
-  __device__ int d() const { return 2 * n * P + 2 * n * kRegRows; }    // pseudo-values
-  __device__ int vv() const { return 2 * n * P + 3 * n * kRegRows; }   // v of the block's rows
-  __device__ int kk() const { return 2 * n * P + 4 * n * kRegRows; }   // k_j.k_t, [n][n]
-  __device__ int kq() const { return kk() + n * n; }                   // k_j.q_t
-  __device__ int gam() const { return kq() + n * n; }
-  __device__ int bet() const { return gam() + n; }
-  __device__ int total() const { return bet() + n; }
+struct WyPlan {
+  static constexpr int KB = DK / 64;                       // 64-column blocks of a vector
+  static constexpr int kPieces = 0;                        // 3*KB tiles: piece p, block kb
+  static constexpr int kNodes = 3 * KB * kWyTile;          // KB tiles: k rows, then q rows
+  static constexpr int kStage = 4 * KB * kWyTile;          // the float rows as copied in
+  static constexpr int kRegion = 4 * KB * kWyTile + kWyRows * DK * 4;
+  // after the MMAs (the operands and staging are dead): per-row values, node tables
+  static constexpr int kA = 0;                             // v_t - gamma_t (S0 k_t), [node][row]
+  static constexpr int kB = kWyMaxNodes * kWyRows * 4;     // S0 q_t
+  static constexpr int kD = 2 * kWyMaxNodes * kWyRows * 4; // pseudo-values d_t
+  static constexpr int kG = 3 * kWyMaxNodes * kWyRows * 4; // (gamma_t/gamma_j) k_j.k_t, [t][j]
+  static constexpr int kHq = kG + kWyMaxNodes * kWyMaxNodes * 4;  // (gamma_t/gamma_j) k_j.q_t
+  static constexpr int kTablesEnd = kHq + kWyMaxNodes * kWyMaxNodes * 4;
+  static constexpr int kMisc = kRegion > kTablesEnd ? kRegion : kTablesEnd;
+  // misc: path lists (node t: t, parent, ..., the node below the root; int32), lengths,
+  // gamma, beta, alpha, parents, two barriers, the tensor-memory address, a flag
+  static constexpr int kPath = kMisc;
+  static constexpr int kLen = kPath + kWyMaxNodes * kWyMaxNodes * 4;
+  static constexpr int kGam = kLen + kWyMaxNodes;
+  static constexpr int kBet = kGam + kWyMaxNodes * 4;
+  static constexpr int kAlp = kBet + kWyMaxNodes * 4;
+  static constexpr int kPar = kAlp + kWyMaxNodes * 4;
+  static constexpr int kBar = kPar + kWyMaxNodes * 4;      // staging barrier, MMA barrier
+  static constexpr int kTmem = kBar + 16;
+  static constexpr int kFlag = kTmem + 4;
+  static constexpr int kBytes = kFlag + 12;
+  static_assert(kA + 3 * kWyMaxNodes * kWyRows * 4 <= kG, "per-row values overlap the tables");
+  static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
 
-size_t wy_smem(int64_t dk, int64_t n) {
-  const int64_t P = 4 * (dk / 4 + 4);
-  return (size_t)(2 * n * P + 4 * n * kRegRows + 2 * n * n + 2 * n) * 4 + (size_t)n * 4;
+__device__ __forceinline__ uint32_t pack_bf16(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+template <int DK>
+__global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
+    const float* __restrict__ S0, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const uint16_t* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
+    const int32_t* __restrict__ parent, int n, int64_t H, int64_t dv, float* __restrict__ O,
+    int32_t* __restrict__ status) {
+  using P = WyPlan<DK>;
+  constexpr int KB = P::KB;
+  extern __shared__ __align__(1024) uint8_t wsm_tc[];
+  uint8_t* sm = wsm_tc;
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kWyRows;
+  const int rows = (int)(dv - r0 < kWyRows ? dv - r0 : kWyRows);
+  const int n16 = (n + 15) & ~15;
+  int32_t* path = reinterpret_cast<int32_t*>(sm + P::kPath);
+  uint8_t* plen = sm + P::kLen;
+  float* gam = reinterpret_cast<float*>(sm + P::kGam);
+  float* bet = reinterpret_cast<float*>(sm + P::kBet);
+  float* alp = reinterpret_cast<float*>(sm + P::kAlp);
+  int32_t* par = reinterpret_cast<int32_t*>(sm + P::kPar);
+  const uint32_t bar_stage = sbase + P::kBar, bar_mma = bar_stage + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P::kTmem);
+  int32_t* flag = reinterpret_cast<int32_t*>(sm + P::kFlag);
+
+  // ---- inputs: the head's state rows by one bulk copy, node scalars, node vectors
+  if (tid == 0) {
+    *flag = 0;
+    mbar_init(bar_stage, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)rows * DK * 4;
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(bar_stage, bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(S0 + (h * dv + r0) * DK);
+    for (uint32_t off = 0; off < bytes; off += 16384u)
+      bulk_g2s(sbase + P::kStage + off, src + off, bytes - off < 16384u ? bytes - off : 16384u, bar_stage, pol);
+  }
+  // rows past dv read as zero (their lanes are never stored)
+  for (int e = rows * DK + tid; e < kWyRows * DK; e += kWyThreads) reinterpret_cast<float*>(sm + P::kStage)[e] = 0.f;
+  for (int t = tid; t < n; t += kWyThreads) {
+    par[t] = parent[t];
+    alp[t] = alpha[(int64_t)t * H + h];
+    bet[t] = beta[(int64_t)t * H + h];
+  }
+  // node tiles: rows 0..n16-1 hold k_t, rows n16..2*n16-1 q_t, the rest zero
+  for (int u = tid; u < KB * kWyRows * 8; u += kWyThreads) {
+    const int kb = u / (kWyRows * 8), R = (u / 8) % kWyRows, c8 = u & 7;
+    const uint16_t* src = nullptr;
+    if (R < n16) {
+      if (R < n) src = k + ((int64_t)R * H + h) * DK;
+    } else if (R < 2 * n16 && R - n16 < n) {
+      src = q + ((int64_t)(R - n16) * H + h) * DK;
+    }
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (src) {
+      src += kb * 64 + c8 * 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = pack_bf16(src[2 * i], src[2 * i + 1]);
+    }
+    sts128(sbase + P::kNodes + kb * kWyTile + R * 128 + ((c8 ^ (R & 7)) << 4), w[0], w[1], w[2], w[3]);
+  }
+  __syncthreads();
+  // ---- the tree: parents checked, each node's path to the root and gamma (root side first)
+  if (tid < n) {
+    const int t = tid;
+    bool ok = t == 0 ? par[0] == -1 : (par[t] >= 0 && par[t] < t);
+    int L = 0;
+    if (ok)
+      for (int j = t; j > 0; j = par[j]) {
+        if (par[j] < 0 || par[j] >= j) {  // an ancestor's bad parent (also flagged by that node)
+          ok = false;
+          break;
+        }
+        path[t * kWyMaxNodes + L++] = j;
+      }
+    if (!ok) atomicOr(flag, 1);
+    plen[t] = (uint8_t)L;
+    float g = 1.f;
+    for (int i = L - 1; i >= 0; --i) g = alp[path[t * kWyMaxNodes + i]] * g;
+    gam[t] = g;
+  }
+  const bool landed = mbar_wait_bounded(bar_stage, 0u);
+  if (!landed) atomicOr(flag, 4);
+  __syncthreads();
+  if (*flag) {
+    if (tid == 0) {
+      if (blockIdx.y == 0 && (*flag & 1)) atomicOr(status, 1);
+      if (*flag & 4) atomicOr(status, 4);
+    }
+    return;  // no tensor memory held yet; a copy that did not land in a second is abandoned
+  }
+  // ---- the three pieces of every state element, in the A operand's swizzled layout
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tslot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  {
+    const float* st = reinterpret_cast<const float*>(sm + P::kStage);
+    for (int u = tid; u < KB * kWyRows * 8; u += kWyThreads) {
+      const int R = u / (KB * 8), kb = (u / 8) % KB, c8 = u & 7;
+      const float4 f0 = *reinterpret_cast<const float4*>(st + R * DK + kb * 64 + c8 * 8);
+      const float4 f1 = *reinterpret_cast<const float4*>(st + R * DK + kb * 64 + c8 * 8 + 4);
+      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+      uint16_t p1[8], p2[8], p3[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        p1[i] = bf16_rne(f[i]);
+        const float e1 = __fsub_rn(f[i], bf16v(p1[i]));
+        p2[i] = bf16_rne(e1);
+        p3[i] = bf16_rne(__fsub_rn(e1, bf16v(p2[i])));
+      }
+      const uint32_t off = R * 128 + ((c8 ^ (R & 7)) << 4);
+      const uint32_t a0 = sbase + P::kPieces + kb * kWyTile + off;
+      sts128(a0, pack_bf16(p1[0], p1[1]), pack_bf16(p1[2], p1[3]), pack_bf16(p1[4], p1[5]), pack_bf16(p1[6], p1[7]));
+      sts128(a0 + KB * kWyTile, pack_bf16(p2[0], p2[1]), pack_bf16(p2[2], p2[3]), pack_bf16(p2[4], p2[5]),
+             pack_bf16(p2[6], p2[7]));
+      sts128(a0 + 2 * KB * kWyTile, pack_bf16(p3[0], p3[1]), pack_bf16(p3[2], p3[3]), pack_bf16(p3[4], p3[5]),
+             pack_bf16(p3[6], p3[7]));
+    }
+  }
+  fence_proxy_async_smem();  // the generic-proxy operand stores -> the tensor core's reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  // ---- D1[row][c] = pieces . [k | q]^T (columns 0..2*n16), D2[i][j] = [k | q]_i . k_j
+  if (tid == 0) {
+    const uint32_t id1 = umma_idesc_n((uint32_t)(2 * n16)), id2 = umma_idesc_n((uint32_t)n16);
+    for (int p = 0; p < 3; ++p)
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint64_t ad = umma_desc(sbase + P::kPieces + (p * KB + kb) * kWyTile);
+        const uint64_t bd = umma_desc(sbase + P::kNodes + kb * kWyTile);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, id1, (p | kb | ks) ? 1u : 0u);
+      }
+    for (int kb = 0; kb < KB; ++kb) {
+      const uint64_t nd = umma_desc(sbase + P::kNodes + kb * kWyTile);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + 128, nd + 2 * ks, nd + 2 * ks, id2, (kb | ks) ? 1u : 0u);
+    }
+    umma_commit(bar_mma);
+  }
+  const bool done = mbar_wait_bounded(bar_mma, 0u);
+  tc_fence_after();
+  if (!done) atomicOr(flag, 4);
+  // ---- read back: warps 0-3 the state products (lane = state row), warps 4-7 the tables
+  float* A_s = reinterpret_cast<float*>(sm + P::kA);
+  float* B_s = reinterpret_cast<float*>(sm + P::kB);
+  float* D_s = reinterpret_cast<float*>(sm + P::kD);
+  float* G = reinterpret_cast<float*>(sm + P::kG);
+  float* Hq = reinterpret_cast<float*>(sm + P::kHq);
+  if (done && warp < 4) {
+    const int R = warp * 32 + lane;
+    const bool live = R < rows;
+    for (int c0 = 0; c0 < 2 * n16; c0 += 16) {
+      float val[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, val);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i;
+        if (c < n16) {
+          if (c < n) {
+            const float vt = live ? bf16v(v[((int64_t)c * H + h) * dv + r0 + R]) : 0.f;
+            A_s[c * kWyRows + R] = vt - gam[c] * val[i];
+          }
+        } else if (c - n16 < n) {
+          B_s[(c - n16) * kWyRows + R] = val[i];
+        }
+      }
+    }
+  } else if (done && warp < 8) {
+    const int i = (warp - 4) * 32 + lane;  // D2 lane: k row i (i < n16) or q row i - n16
+    const bool isk = i < n16;
+    const int t = isk ? i : i - n16;
+    const bool use = t < n && i < 2 * n16;
+    for (int c0 = 0; c0 < n16; c0 += 16) {
+      float val[16];
+      tmem_ld16(tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16) + (uint32_t)c0, val);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const int j = c0 + x;
+        if (use && j < n) (isk ? G : Hq)[t * kWyMaxNodes + j] = (gam[t] / gam[j]) * val[x];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
+  if (!done) {
+    if (tid == 0) atomicOr(status, 4);
+    return;
+  }
+  // ---- pseudo-values, node order, one thread per state row
+  if (tid < kWyRows) {
+    const int R = tid;
+    D_s[R] = 0.f;  // the root has no update here
+    for (int t = 1; t < n; ++t) {
+      // the ancestors' terms in four independent partial sums, so their loads overlap
+      const int32_t* pt = path + t * kWyMaxNodes;
+      const float* Gt = G + t * kWyMaxNodes;
+      const int L = plen[t];
+      float s0 = A_s[t * kWyRows + R], s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int x = 1;
+      for (; x + 4 <= L; x += 4) {
+        const int j0 = pt[x], j1 = pt[x + 1], j2 = pt[x + 2], j3 = pt[x + 3];
+        s0 = fmaf(-Gt[j0], D_s[j0 * kWyRows + R], s0);
+        s1 = fmaf(-Gt[j1], D_s[j1 * kWyRows + R], s1);
+        s2 = fmaf(-Gt[j2], D_s[j2 * kWyRows + R], s2);
+        s3 = fmaf(-Gt[j3], D_s[j3 * kWyRows + R], s3);
+      }
+      for (; x < L; ++x) s0 = fmaf(-Gt[pt[x]], D_s[pt[x] * kWyRows + R], s0);
+      D_s[t * kWyRows + R] = bet[t] * ((s0 + s1) + (s2 + s3));
+    }
+  }
+  __syncthreads();
+  // ---- outputs: thread (row, part) takes the nodes t = part, part + 4, ...
+  {
+    const int R = tid & (kWyRows - 1);
+    if (R < rows)
+      for (int t = tid >> 7; t < n; t += kWyThreads / kWyRows) {
+        const int32_t* pt = path + t * kWyMaxNodes;
+        const float* Ht = Hq + t * kWyMaxNodes;
+        const int L = plen[t];
+        float s0 = gam[t] * B_s[t * kWyRows + R], s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int x = 0;
+        for (; x + 4 <= L; x += 4) {
+          const int j0 = pt[x], j1 = pt[x + 1], j2 = pt[x + 2], j3 = pt[x + 3];
+          s0 = fmaf(Ht[j0], D_s[j0 * kWyRows + R], s0);
+          s1 = fmaf(Ht[j1], D_s[j1 * kWyRows + R], s1);
+          s2 = fmaf(Ht[j2], D_s[j2 * kWyRows + R], s2);
+          s3 = fmaf(Ht[j3], D_s[j3 * kWyRows + R], s3);
+        }
+        for (; x < L; ++x) s0 = fmaf(Ht[pt[x]], D_s[pt[x] * kWyRows + R], s0);
+        O[((int64_t)t * H + h) * dv + r0 + R] = (s0 + s1) + (s2 + s3);
+      }
+  }
 }
 
 template <int DK>
-__global__ void __launch_bounds__(kRegThreads) k_gdn_wy_verify(
-    const float* __restrict__ S0, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
-    const uint16_t* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
-    const int32_t* __restrict__ parent, int64_t n64, int64_t H, int64_t dv, float* __restrict__ O,
-    int32_t* __restrict__ status) {
-  extern __shared__ __align__(16) float wsm[];
-  __shared__ int32_t ok_sh;
-  const int n = (int)n64;
-  const WyLayout<DK> Lw{n};
-  int32_t* par = reinterpret_cast<int32_t*>(wsm + Lw.total());
-  const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kRegRows;
-  const int tid = threadIdx.x, p = tid & 3;
-  const int r = tid >> 2;
-  for (int t = tid; t < n; t += blockDim.x) par[t] = parent[t];
-  if (tid == 0) ok_sh = 1;
-  __syncthreads();
-  if (tid == 0) {
-    bool ok = par[0] == -1;
-    for (int t = 1; ok && t < n; ++t) ok = par[t] >= 0 && par[t] < t;
-    if (!ok) {
-      if (blockIdx.y == 0) atomicOr(status, 1);
-      ok_sh = 0;
-    } else {
-      float* g = wsm + Lw.gam();
-      g[0] = 1.f;  // the committed root: its update is already in S0
-      for (int t = 1; t < n; ++t) g[t] = alpha[(int64_t)t * H + h] * g[par[t]];
-    }
-  }
-  // node vectors (padded so the four quarters of k and q sit on distinct banks), v, beta
-  for (int e = tid; e < n * DK; e += blockDim.x) {
-    const int t = e / DK, c = e - t * DK;
-    wsm[Lw.kpad() + t * WyLayout<DK>::P + vpos<DK>(c)] = bf16v(k[((int64_t)t * H + h) * DK + c]);
-    wsm[Lw.qpad() + t * WyLayout<DK>::P + vpos<DK>(c)] = bf16v(q[((int64_t)t * H + h) * DK + c]);
-  }
-  for (int e = tid; e < n * kRegRows; e += blockDim.x) {
-    const int t = e / kRegRows, rr = e - t * kRegRows;
-    wsm[Lw.vv() + e] = r0 + rr < dv ? bf16v(v[((int64_t)t * H + h) * dv + r0 + rr]) : 0.f;
-  }
-  for (int t = tid; t < n; t += blockDim.x) wsm[Lw.bet() + t] = beta[(int64_t)t * H + h];
-  RegState<DK> S;
-  reg_load<DK>(S, S0 + (h * dv + r0) * DK, dv - r0);
-  __syncthreads();
-  if (!ok_sh) return;
-  // S0 k_t and S0 q_t of this block's rows, every node
-  for (int t = 0; t < n; ++t) {
-    const float at = reg_dot<DK>(S, wsm + Lw.kpad() + t * WyLayout<DK>::P);
-    const float bt = reg_dot<DK>(S, wsm + Lw.qpad() + t * WyLayout<DK>::P);
-    if (p == 0) {
-      wsm[Lw.a() + t * kRegRows + r] = at;
-      wsm[Lw.b() + t * kRegRows + r] = bt;
-    }
-  }
-  // (gamma_t/gamma_j) k_j.k_t and (gamma_t/gamma_j) k_j.q_t for j <= t (the four quarters
-  // of each padded vector, skipping the padding)
-  {
-    const float* gm = wsm + Lw.gam();
-    constexpr int Q = RegState<DK>::Q;
-    for (int e = tid; e < n * n; e += blockDim.x) {
-      const int t = e / n, j = e - t * n;
-      if (j > t) continue;
-      const float* kj = wsm + Lw.kpad() + j * WyLayout<DK>::P;
-      const float* kt = wsm + Lw.kpad() + t * WyLayout<DK>::P;
-      const float* qt = wsm + Lw.qpad() + t * WyLayout<DK>::P;
-      float g0 = 0.f, g1 = 0.f;
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq)
-        for (int m = 0; m < Q; ++m) {
-          const int c = qq * (Q + 4) + m;
-          g0 = fmaf(kj[c], kt[c], g0);
-          g1 = fmaf(kj[c], qt[c], g1);
-        }
-      const float ratio = gm[t] / gm[j];
-      wsm[Lw.kk() + t * n + j] = ratio * g0;
-      wsm[Lw.kq() + t * n + j] = ratio * g1;
-    }
-  }
-  __syncthreads();
-  // pseudo-values, node order, one thread per row
-  const float* gam = wsm + Lw.gam();
-  if (p == 0) {
-    float* d = wsm + Lw.d();
-    d[r] = 0.f;  // the root has no update here
-    for (int t = 1; t < n; ++t) {
-      float acc = wsm[Lw.vv() + t * kRegRows + r] - gam[t] * wsm[Lw.a() + t * kRegRows + r];
-      for (int j = par[t]; j > 0; j = par[j]) acc = fmaf(-wsm[Lw.kk() + t * n + j], d[j * kRegRows + r], acc);
-      d[t * kRegRows + r] = wsm[Lw.bet() + t] * acc;
-    }
-  }
-  __syncthreads();
-  // outputs: the four threads of a row split the nodes
-  const int64_t row = r0 + r;
-  for (int t = p; t < n; t += 4) {
-    float o = gam[t] * wsm[Lw.b() + t * kRegRows + r];
-    for (int j = t; j > 0; j = par[j]) o = fmaf(wsm[Lw.kq() + t * n + j], wsm[Lw.d() + j * kRegRows + r], o);
-    if (row < dv) O[((int64_t)t * H + h) * dv + row] = o;
-  }
+size_t wy_tc_smem() {
+  return (size_t)WyPlan<DK>::kBytes;
 }
 
 // four threads per state row and a thread per element of k, whole warps
@@ -626,20 +801,19 @@ int gdn_wy_verify(const float* S0, const uint16_t* q, const uint16_t* k, const u
   if (dk != 64 && dk != 128) return fail(W12_ERR_SHAPE, "%s: dk=%lld (64 or 128)", fn, (long long)dk);
   if (n < 1 || n > kWyMaxNodes)
     return fail(W12_ERR_SHAPE, "%s: n=%lld out of range (1..%d)", fn, (long long)n, kWyMaxNodes);
-  if (dv > 65535 * (int64_t)kRegRows) return fail(W12_ERR_SHAPE, "%s: dv=%lld", fn, (long long)dv);
+  if (dv > 65535 * (int64_t)kWyRows) return fail(W12_ERR_SHAPE, "%s: dv=%lld", fn, (long long)dv);
   if (!S0 || !q || !k || !v || !alpha || !beta || !parent || !O || !status)
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if ((((uintptr_t)S0) & 15u) != 0) return fail(W12_ERR_INVALID_ARG, "%s: S0 must be 16-byte aligned", fn);
-  const size_t smem = wy_smem(dk, n);
-  const dim3 grid((unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
+  const dim3 grid((unsigned)H, (unsigned)((dv + kWyRows - 1) / kWyRows));
   if (dk == 128) {
-    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify<128>, smem))) return st;
-    k_gdn_wy_verify<128><<<grid, kRegThreads, smem, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
-                                                                           dv, O, status);
+    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify_tc<128>, wy_tc_smem<128>()))) return st;
+    k_gdn_wy_verify_tc<128><<<grid, kWyThreads, wy_tc_smem<128>(), (cudaStream_t)stream>>>(
+        S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O, status);
   } else {
-    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify<64>, smem))) return st;
-    k_gdn_wy_verify<64><<<grid, kRegThreads, smem, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H, dv,
-                                                                          O, status);
+    if ((st = set_gdn_smem((const void*)k_gdn_wy_verify_tc<64>, wy_tc_smem<64>()))) return st;
+    k_gdn_wy_verify_tc<64><<<grid, kWyThreads, wy_tc_smem<64>(), (cudaStream_t)stream>>>(
+        S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O, status);
   }
   W12_LAUNCH_CHECK(fn);
   return W12_OK;

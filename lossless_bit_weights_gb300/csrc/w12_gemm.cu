@@ -143,7 +143,11 @@ struct TcPlan {
   // 22-warp CTA puts six on one, so 80 registers a thread is the most that launches.
   static constexpr int kBoundThreads = kPipes == 1 ? kCtaThreads : kCtaThreads > 704 ? kCtaThreads : 704;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
-  static constexpr int kXStages = NT <= 64 ? 4 : 2;
+  static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : 2;
+  // A buffers (decoded 128x64 tiles) in rotation over the pipeline's units: with more than
+  // one per decode group, a group stores a unit while the MMA of the unit before its previous
+  // one may still run
+  static constexpr int kABufs = MODE == kModeOwn ? 3 : MODE == kModeOne ? 4 : 2;
   // shared x region (wide): x stages, then x_full[SX] x_empty[SX]
   static constexpr int kXRegion = kWide ? (kXStages * kX + 2 * kXStages * 8 + 1023) / 1024 * 1024 : 0;
   static constexpr int kOffXBar = kXStages * kX;
@@ -153,21 +157,22 @@ struct TcPlan {
   static constexpr int kOffEsc = kHi + kLo;
   static constexpr int kOffHdr = kOffEsc + kEscRun * 4;       // tile_ptr[4u..4u+4], run start
   static constexpr int kRec = kOffHdr + 32;
-  static constexpr int kOffA = kWide ? 0 : kXStages * kX;     // one A buffer per decode group
-  static constexpr int kOffRec = kOffA + kGroups * kABuf;
+  static constexpr int kOffA = kWide ? 0 : kXStages * kX;
+  static constexpr int kOffRec = kOffA + kABufs * kABuf;
   static constexpr int kBudget =
       kWide ? ((227 * 1024 - kXRegion) / 2) / 1024 * 1024 : (MODE == kModeOne ? 224 : 112) * 1024;
   static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
-  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[G] a_empty[G] epi[G] acc_full acc_empty mma_done
-  static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 3 * kGroups + 3;
+  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[AB] a_empty[AB] epi[G] acc_full acc_empty mma_done
+  static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 2 * kABufs + kGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kPipeBytes = (kBytes + 1023) / 1024 * 1024;
   static constexpr int kCtaBytes = kPipes == 1 ? kBytes : kXRegion + kPipes * kPipeBytes;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
   static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
+  static_assert(kABufs >= kGroups, "an A buffer per decode group at least");
   static_assert(kCtaBytes <= 227 * 1024, "shared memory plan too large");
   static_assert((MODE == kModeOwn) == (NT <= 32), "launch mode does not fit the token tile");
   static_assert(kPipes * kTmemCols <= 512, "tensor memory plan too large");
@@ -202,54 +207,9 @@ __device__ __forceinline__ void decode16_i8(uint4 h, uint32_t out[8]) {
   }
 }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128.
-template <int NT>
-__device__ __forceinline__ constexpr uint32_t umma_idesc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 16 fp32 columns of the accumulator (this warp's lane quarter).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  // the registers are operands of the wait, so no use of them is scheduled before it
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Wait for another warp's work on a barrier phase, bounded by c_wait_limit.
 __device__ __forceinline__ bool peer_wait(uint32_t bar, uint32_t parity) {
-  return mbar_wait_bounded(bar, parity, c_wait_limit);
+  return mbar_wait_inline(bar, parity, c_wait_limit);
 }
 
 // Bounded barrier wait whose outcome is the same in every lane of the warp.
@@ -330,7 +290,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   using P = TcPlan<NT, Q8, MODE>;
   constexpr bool I8 = EPI == EPI_I8;  // INT8 codes: no window bases, escapes or lo plane
   static_assert(!I8 || Q8, "INT8 codes use the 8-bit record plan");
-  constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups;
+  constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups, AB = P::kABufs;
   constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
   extern __shared__ __align__(1024) uint8_t smem_cta[];
   const int lane = threadIdx.x & 31, gwarp = threadIdx.x >> 5;
@@ -355,8 +315,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   const uint32_t bar0 = sbase + P::kOffBar;
   const uint32_t rec_full0 = bar0, rec_empty0 = bar0 + 8 * S;
   const uint32_t x_full0 = P::kWide ? xbase + P::kOffXBar : bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
-  const uint32_t a_full0 = bar0 + 16 * S + (P::kWide ? 0 : 16 * SX), a_empty0 = a_full0 + 8 * kTcGroups;
-  const uint32_t epi0 = a_empty0 + 8 * kTcGroups;
+  const uint32_t a_full0 = bar0 + 16 * S + (P::kWide ? 0 : 16 * SX), a_empty0 = a_full0 + 8 * AB;
+  const uint32_t epi0 = a_empty0 + 8 * AB;
   const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
   // misc: [0] TMEM address, [1+g] stream-K flag of group g, [15] drains finished (four per segment)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
@@ -384,11 +344,11 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         mbar_init(x_full0 + 8 * i, 1);
         mbar_init(x_empty0 + 8 * i, P::kWide ? 2 : 1);  // wide: freed by both MMA issuers
       }
-    for (int i = 0; i < kTcGroups; ++i) {
+    for (int i = 0; i < AB; ++i) {
       mbar_init(a_full0 + 8 * i, kBlockTiles * 32);
       mbar_init(a_empty0 + 8 * i, 1);
-      mbar_init(epi0 + 8 * i, kBlockTiles * 32);
     }
+    for (int i = 0; i < kTcGroups; ++i) mbar_init(epi0 + 8 * i, kBlockTiles * 32);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kBlockTiles * 32);
     mbar_init(mma_done, 1);
@@ -543,7 +503,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       const uint64_t ad0 = umma_desc(sbase + P::kOffA), xd0 = umma_desc(xbase);
       const int KC = (int)a.KC;
       int kc = (int)(u0 % a.KC);
-      int seg = 0, s = 0, gi = 0;
+      int seg = 0, s = 0, ab = 0;
       uint32_t xph = 0, aph = 0;
       for (int j = 0; j < nunp; ++j) {
         const bool first = (j == 0) || (kc == 0);
@@ -551,16 +511,16 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           bail = true;
           break;
         }
-        if (!peer_wait(a_full0 + 8 * gi, aph) || !peer_wait(x_full0 + 8 * s, xph)) {
+        if (!peer_wait(a_full0 + 8 * ab, aph) || !peer_wait(x_full0 + 8 * s, xph)) {
           bail = true;
           break;
         }
         tc_fence_after();
-        const uint64_t ad = ad0 + (uint64_t)((gi * kABuf) >> 4), xd = xd0 + (uint64_t)((s * P::kX) >> 4);
+        const uint64_t ad = ad0 + (uint64_t)((ab * kABuf) >> 4), xd = xd0 + (uint64_t)((s * P::kX) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem, ad + 2 * ks, xd + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
-        umma_commit(a_empty0 + 8 * gi);
+        umma_commit(a_empty0 + 8 * ab);
         umma_commit(x_empty0 + 8 * s);
         if (kc + 1 == KC || j + 1 == nunp) {
           umma_commit(acc_full);
@@ -571,8 +531,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           s = 0;
           xph ^= 1u;
         }
-        if (++gi == kTcGroups) {
-          gi = 0;
+        if (++ab == AB) {
+          ab = 0;
           aph ^= 1u;
         }
       }
@@ -602,15 +562,18 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     // 32 bits (the host caps T).
     const int gi = warp >> 2, tl = warp & 3;  // group, row tile inside the block
     const int g = lane >> 2, t = lane & 3;
-    uint8_t* atp = smem + P::kOffA + gi * kABuf + tl * (kTileRows * 128);
-    const uint32_t a_full = a_full0 + 8 * gi, a_empty = a_empty0 + 8 * gi, epi_bar = epi0 + 8 * gi;
+    // unit j decodes into A buffer j % AB; au counts the buffer's earlier uses (its phase)
+    uint8_t* const abase = smem + P::kOffA + tl * (kTileRows * 128);
+    const uint32_t epi_bar = epi0 + 8 * gi;
+    int ab = gi % AB;
+    uint32_t au = (uint32_t)(gi / AB);
     const int KC = (int)a.KC, U0 = (int)u0;
     const int srb0 = U0 / KC;
     int j = gi;
     int srb = (U0 + j) / KC, kc = (U0 + j) - srb * KC;  // partition row (row block or pair) and chunk
     int s = j % S;
     uint32_t ph = (uint32_t)((j / S) & 1);
-    int cur_rb = -1, mine = 0;
+    int cur_rb = -1;
     uint32_t base2[4];
     uint32_t epi_phase = 0;
     for (; j < nunp; j += kTcGroups) {
@@ -661,9 +624,12 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         }
         // the record stage can be refilled now (every thread arrives once its own loads are done)
         mbar_arrive(rec_empty0 + 8 * s);
-        // the group's A buffer is free once the MMA of its previous unit has finished (issued
-        // while the other group decoded, so this wait rarely blocks)
-        if (mine > 0 && !warp_wait(a_empty, (uint32_t)((mine - 1) & 1))) {
+        // the A buffer is free once the MMA of its previous unit (j - AB) has finished.  The
+        // parity wait is exact: that MMA's phase is the buffer's latest unless the one before
+        // (unit j - 2 AB) is still open, and it is not: this group waited for unit j - 2 - AB
+        // before its previous unit, and MMAs complete in issue order.
+        uint8_t* const atp = abase + ab * kABuf;
+        if (au > 0 && !warp_wait(a_empty0 + 8 * ab, (au - 1) & 1u)) {
           bail = true;
           break;
         }
@@ -689,8 +655,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           }
         }
         fence_proxy_async_smem();  // this thread's generic-proxy stores -> tensor-core reads
-        mbar_arrive(a_full);
-        ++mine;
+        mbar_arrive(a_full0 + 8 * ab);
       }
       if (kc == KC - 1 || j == nunp - 1) {
         // ---- this unit ends a row block (or the CTA's share of one): the accumulator
@@ -781,7 +746,12 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           }
         }
       }
-      // G units on (S > G, so the ring wraps at most once)
+      // G units on (S > G and AB >= G, so the ring and the buffers wrap at most once)
+      ab += kTcGroups;
+      if (ab >= AB) {
+        ab -= AB;
+        ++au;
+      }
       s += kTcGroups;
       if (s >= S) {
         s -= S;
