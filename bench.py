@@ -562,6 +562,28 @@ def timed_ms(torch, fn, n, warm=3):
     return a.elapsed_time(b) / n
 
 
+def graph_ms(torch, fn, n, warm=3):
+    """Average ms of one replay of a CUDA graph that holds one call of fn (device time of
+    a launch sequence whose kernels are shorter than the host's launch overhead)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(n):
+        g.replay()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
 def gemm_bytes(A, M, q8=False):
     return A.stream_bytes(q8=q8) + 2 * M * A.K + 4 * M * A.N
 
@@ -884,14 +906,26 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
         for Lg in layers_g:
             w12.gdn_wy_verify(Lg["S"], Lg["q"], Lg["k"], Lg["v"], Lg["a"], Lg["b"], par_g, O=Lg["O"], status=st_g)
 
-    ms_v = timed_ms(torch, gdn_verify_all, steps)
-    ms_wy = timed_ms(torch, gdn_wy_all, steps)
-    ms_c = timed_ms(torch, gdn_commit_all, steps)      # each call advances the states further
+    # 48 launches of a few microseconds each: eager timing measures the host's launch rate,
+    # so the device time comes from replaying the 48 launches captured in a CUDA graph
+    ms_v_e = timed_ms(torch, gdn_verify_all, steps)
+    ms_wy_e = timed_ms(torch, gdn_wy_all, steps)
+    ms_v = graph_ms(torch, gdn_verify_all, steps)
+    ms_wy = graph_ms(torch, gdn_wy_all, steps)
+    ms_c = graph_ms(torch, gdn_commit_all, steps)      # each call advances the states further
     for Lg, S0g in zip(layers_g, S_keep):
         Lg["S"].copy_(S0g)
+    # the WY launch's algorithmic bytes: the float state, the node vectors and scalars, the tree
+    # and the outputs (the state products are 2 H dv dk 2n flops, small beside the bytes)
+    wy_bytes = n_l * (Hg * dg * dg * 4 + nn * Hg * (2 * dg * 2 + dg * 2 + 8) + nn * 4 + nn * Hg * dg * 4)
     out["gdn_verify_48x32"] = {"layers": n_l, "heads": Hg, "dk": dg, "dv": dg, "tree_nodes": nn,
                                "accepted": len(acc_nodes) - 1, "path_verify_us": 1e3 * ms_v,
                                "wy_verify_us": 1e3 * ms_wy, "commit_us": 1e3 * ms_c,
+                               "timing": "CUDA-graph replay of the 48 launches",
+                               "path_verify_eager_us": 1e3 * ms_v_e, "wy_verify_eager_us": 1e3 * ms_wy_e,
+                               "wy_stream_GBps": wy_bytes / (ms_wy * 1e-3) / 1e9,
+                               "wy_frac_hbm": wy_bytes / (ms_wy * 1e-3) / 1e9 / hbm,
+                               "wy_kernel": "tcgen05 bf16 MMAs over the state's three exact bf16 pieces",
                                "step_us": 1e3 * (min(ms_v, ms_wy) + ms_c),
                                "snapshot_bytes_avoided": n_l * nn * Hg * dg * dg * 4,
                                "status": int(st_g.item())}

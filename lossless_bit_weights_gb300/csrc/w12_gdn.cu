@@ -12,6 +12,7 @@
 // so one step is a row dot u = S k and a rank-1 write
 //     S <- alpha S + (beta v - alpha beta u) k^T.
 #include <cstdint>
+#include <mutex>
 
 #include "w12_internal.cuh"
 
@@ -427,8 +428,8 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_commit_reg(
 // One CTA per (head, 128 state rows): the rows arrive by one bulk copy, 16 warps split them
 // into the three pieces in the operands' 128-byte-swizzled layout, one thread issues the
 // MMAs (accumulators in tensor memory), four warps read the state products back (lane =
-// state row) and four the node tables, four warps run the substitution and all sixteen
-// the outputs.
+// state row) and four the node tables, and four warps run the substitution and the outputs
+// with each row's pseudo-values in registers.
 constexpr int kWyMaxNodes = 64;
 constexpr int kWyRows = 128;                 // state rows per CTA: the MMA's M
 constexpr int kWyThreads = 512;
@@ -444,16 +445,14 @@ struct WyPlan {
   // after the MMAs (the operands and staging are dead): per-row values, node tables
   static constexpr int kA = 0;                             // v_t - gamma_t (S0 k_t), [node][row]
   static constexpr int kB = kWyMaxNodes * kWyRows * 4;     // S0 q_t
-  static constexpr int kD = 2 * kWyMaxNodes * kWyRows * 4; // pseudo-values d_t
   static constexpr int kG = 3 * kWyMaxNodes * kWyRows * 4; // (gamma_t/gamma_j) k_j.k_t, [t][j]
   static constexpr int kHq = kG + kWyMaxNodes * kWyMaxNodes * 4;  // (gamma_t/gamma_j) k_j.q_t
   static constexpr int kTablesEnd = kHq + kWyMaxNodes * kWyMaxNodes * 4;
   static constexpr int kMisc = kRegion > kTablesEnd ? kRegion : kTablesEnd;
-  // misc: path lists (node t: t, parent, ..., the node below the root; int32), lengths,
-  // gamma, beta, alpha, parents, two barriers, the tensor-memory address, a flag
+  // misc: each node's path as a bit mask over the nodes (t and its ancestors below the
+  // root), gamma, beta, alpha, parents, two barriers, the tensor-memory address, a flag
   static constexpr int kPath = kMisc;
-  static constexpr int kLen = kPath + kWyMaxNodes * kWyMaxNodes * 4;
-  static constexpr int kGam = kLen + kWyMaxNodes;
+  static constexpr int kGam = kPath + kWyMaxNodes * 8;
   static constexpr int kBet = kGam + kWyMaxNodes * 4;
   static constexpr int kAlp = kBet + kWyMaxNodes * 4;
   static constexpr int kPar = kAlp + kWyMaxNodes * 4;
@@ -482,8 +481,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
   const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kWyRows;
   const int rows = (int)(dv - r0 < kWyRows ? dv - r0 : kWyRows);
   const int n16 = (n + 15) & ~15;
-  int32_t* path = reinterpret_cast<int32_t*>(sm + P::kPath);
-  uint8_t* plen = sm + P::kLen;
+  unsigned long long* pmask = reinterpret_cast<unsigned long long*>(sm + P::kPath);
   float* gam = reinterpret_cast<float*>(sm + P::kGam);
   float* bet = reinterpret_cast<float*>(sm + P::kBet);
   float* alp = reinterpret_cast<float*>(sm + P::kAlp);
@@ -533,23 +531,24 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     sts128(sbase + P::kNodes + kb * kWyTile + R * 128 + ((c8 ^ (R & 7)) << 4), w[0], w[1], w[2], w[3]);
   }
   __syncthreads();
-  // ---- the tree: parents checked, each node's path to the root and gamma (root side first)
+  // ---- the tree: parents checked, each node's path as a mask, gamma (root side first: a
+  // parent's index is below its child's, so rising bit order walks the path from the root)
   if (tid < n) {
     const int t = tid;
     bool ok = t == 0 ? par[0] == -1 : (par[t] >= 0 && par[t] < t);
-    int L = 0;
+    unsigned long long m = 0ull;
     if (ok)
       for (int j = t; j > 0; j = par[j]) {
         if (par[j] < 0 || par[j] >= j) {  // an ancestor's bad parent (also flagged by that node)
           ok = false;
           break;
         }
-        path[t * kWyMaxNodes + L++] = j;
+        m |= 1ull << j;
       }
     if (!ok) atomicOr(flag, 1);
-    plen[t] = (uint8_t)L;
+    pmask[t] = m;
     float g = 1.f;
-    for (int i = L - 1; i >= 0; --i) g = alp[path[t * kWyMaxNodes + i]] * g;
+    for (unsigned long long r = m; r; r &= r - 1) g = alp[__ffsll((long long)r) - 1] * g;
     gam[t] = g;
   }
   const bool landed = mbar_wait_bounded(bar_stage, 0u);
@@ -614,46 +613,59 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     }
     umma_commit(bar_mma);
   }
+  // v of this thread's state row for every node, loaded while the MMAs run (warps 0-3)
+  const int Rw = (warp & 3) * 32 + lane;
+  float vr[kWyMaxNodes];
+  if (warp < 4) {
+#pragma unroll
+    for (int c = 0; c < kWyMaxNodes; ++c)
+      vr[c] = (c < n && Rw < rows) ? bf16v(v[((int64_t)c * H + h) * dv + r0 + Rw]) : 0.f;
+  }
   const bool done = mbar_wait_bounded(bar_mma, 0u);
   tc_fence_after();
   if (!done) atomicOr(flag, 4);
-  // ---- read back: warps 0-3 the state products (lane = state row), warps 4-7 the tables
+  // ---- read back: warps 0-3 the state products (lane = state row), warps 4-7 the node
+  // tables, kept only on each node's path (zero elsewhere, so the solve below runs dense)
   float* A_s = reinterpret_cast<float*>(sm + P::kA);
   float* B_s = reinterpret_cast<float*>(sm + P::kB);
-  float* D_s = reinterpret_cast<float*>(sm + P::kD);
   float* G = reinterpret_cast<float*>(sm + P::kG);
   float* Hq = reinterpret_cast<float*>(sm + P::kHq);
   if (done && warp < 4) {
-    const int R = warp * 32 + lane;
-    const bool live = R < rows;
-    for (int c0 = 0; c0 < 2 * n16; c0 += 16) {
-      float val[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, val);
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = c0 + i;
-        if (c < n16) {
-          if (c < n) {
-            const float vt = live ? bf16v(v[((int64_t)c * H + h) * dv + r0 + R]) : 0.f;
-            A_s[c * kWyRows + R] = vt - gam[c] * val[i];
-          }
-        } else if (c - n16 < n) {
-          B_s[(c - n16) * kWyRows + R] = val[i];
+    for (int c0 = 0; c0 < kWyMaxNodes; c0 += 16) {
+      if (c0 < n16) {
+        float val[16];
+        tmem_ld16(tmem + lanes + (uint32_t)c0, val);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 + i;
+          if (c < n) A_s[c * kWyRows + Rw] = vr[c] - gam[c] * val[i];
         }
       }
+    }
+    for (int c0 = 0; c0 < n16; c0 += 16) {
+      float val[16];
+      tmem_ld16(tmem + lanes + (uint32_t)(n16 + c0), val);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < n) B_s[(c0 + i) * kWyRows + Rw] = val[i];
     }
   } else if (done && warp < 8) {
     const int i = (warp - 4) * 32 + lane;  // D2 lane: k row i (i < n16) or q row i - n16
     const bool isk = i < n16;
     const int t = isk ? i : i - n16;
     const bool use = t < n && i < 2 * n16;
+    const unsigned long long m = use ? pmask[t] : 0ull;
     for (int c0 = 0; c0 < n16; c0 += 16) {
       float val[16];
       tmem_ld16(tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16) + (uint32_t)c0, val);
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         const int j = c0 + x;
-        if (use && j < n) (isk ? G : Hq)[t * kWyMaxNodes + j] = (gam[t] / gam[j]) * val[x];
+        // k rows: the ancestors of t below the root; q rows: t and those ancestors
+        const bool on = ((m >> j) & 1ull) && (!isk || j != t);
+        if (use && j < n) (isk ? G : Hq)[t * kWyMaxNodes + j] = on ? (gam[t] / gam[j]) * val[x] : 0.f;
       }
     }
   }
@@ -665,49 +677,36 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     if (tid == 0) atomicOr(status, 4);
     return;
   }
-  // ---- pseudo-values, node order, one thread per state row
+  // ---- pseudo-values and outputs, node order, one thread per state row, the pseudo-values
+  // in registers.  The tables are zero off each node's path, so the sums run over every
+  // earlier node without indirection; each node's output follows its pseudo-value and fills
+  // the latency of the next one's chain.
   if (tid < kWyRows) {
     const int R = tid;
-    D_s[R] = 0.f;  // the root has no update here
-    for (int t = 1; t < n; ++t) {
-      // the ancestors' terms in four independent partial sums, so their loads overlap
-      const int32_t* pt = path + t * kWyMaxNodes;
+    const bool live = R < rows;
+    float d[kWyMaxNodes];
+    d[0] = 0.f;  // the root has no update here
+    if (live) O[(int64_t)h * dv + r0 + R] = gam[0] * B_s[R];
+#pragma unroll
+    for (int t = 1; t < kWyMaxNodes; ++t) {
+      if (t >= n) break;
       const float* Gt = G + t * kWyMaxNodes;
-      const int L = plen[t];
       float s0 = A_s[t * kWyRows + R], s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      int x = 1;
-      for (; x + 4 <= L; x += 4) {
-        const int j0 = pt[x], j1 = pt[x + 1], j2 = pt[x + 2], j3 = pt[x + 3];
-        s0 = fmaf(-Gt[j0], D_s[j0 * kWyRows + R], s0);
-        s1 = fmaf(-Gt[j1], D_s[j1 * kWyRows + R], s1);
-        s2 = fmaf(-Gt[j2], D_s[j2 * kWyRows + R], s2);
-        s3 = fmaf(-Gt[j3], D_s[j3 * kWyRows + R], s3);
+#pragma unroll
+      for (int j = 1; j < t; ++j) {
+        float& acc = (j & 3) == 0 ? s0 : (j & 3) == 1 ? s1 : (j & 3) == 2 ? s2 : s3;
+        acc = fmaf(-Gt[j], d[j], acc);
       }
-      for (; x < L; ++x) s0 = fmaf(-Gt[pt[x]], D_s[pt[x] * kWyRows + R], s0);
-      D_s[t * kWyRows + R] = bet[t] * ((s0 + s1) + (s2 + s3));
+      d[t] = bet[t] * ((s0 + s1) + (s2 + s3));
+      const float* Ht = Hq + t * kWyMaxNodes;
+      float o0 = gam[t] * B_s[t * kWyRows + R], o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+      for (int j = 1; j <= t; ++j) {
+        float& acc = (j & 3) == 0 ? o0 : (j & 3) == 1 ? o1 : (j & 3) == 2 ? o2 : o3;
+        acc = fmaf(Ht[j], d[j], acc);
+      }
+      if (live) O[((int64_t)t * H + h) * dv + r0 + R] = (o0 + o1) + (o2 + o3);
     }
-  }
-  __syncthreads();
-  // ---- outputs: thread (row, part) takes the nodes t = part, part + 4, ...
-  {
-    const int R = tid & (kWyRows - 1);
-    if (R < rows)
-      for (int t = tid >> 7; t < n; t += kWyThreads / kWyRows) {
-        const int32_t* pt = path + t * kWyMaxNodes;
-        const float* Ht = Hq + t * kWyMaxNodes;
-        const int L = plen[t];
-        float s0 = gam[t] * B_s[t * kWyRows + R], s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int x = 0;
-        for (; x + 4 <= L; x += 4) {
-          const int j0 = pt[x], j1 = pt[x + 1], j2 = pt[x + 2], j3 = pt[x + 3];
-          s0 = fmaf(Ht[j0], D_s[j0 * kWyRows + R], s0);
-          s1 = fmaf(Ht[j1], D_s[j1 * kWyRows + R], s1);
-          s2 = fmaf(Ht[j2], D_s[j2 * kWyRows + R], s2);
-          s3 = fmaf(Ht[j3], D_s[j3 * kWyRows + R], s3);
-        }
-        for (; x < L; ++x) s0 = fmaf(Ht[pt[x]], D_s[pt[x] * kWyRows + R], s0);
-        O[((int64_t)t * H + h) * dv + r0 + R] = (s0 + s1) + (s2 + s3);
-      }
   }
 }
 
@@ -738,8 +737,29 @@ int check_gdn_dims(int64_t H, int64_t dk, int64_t dv, const char* fn) {
   return W12_OK;
 }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device) unless a larger size is asked for later.
 int set_gdn_smem(const void* kernel, size_t bytes) {
+  struct Entry {
+    const void* k;
+    int dev;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static Entry done[32];
+  static int n_done = 0;
+  int dev = 0;
+  W12_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].k == kernel && done[i].dev == dev && done[i].bytes >= bytes) return W12_OK;
   W12_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].k == kernel && done[i].dev == dev) {
+      done[i].bytes = bytes;
+      return W12_OK;
+    }
+  if (n_done < 32) done[n_done++] = Entry{kernel, dev, bytes};
   return W12_OK;
 }
 
