@@ -46,8 +46,24 @@ HBM_FALLBACK = 6800.0
 # the same metric on both arms (the driver divides one by the other)
 METRIC = "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (34816x5120, M=16)
-# from an ncu capture of the current kernel; None when the kernel changed since.
-TRAFFIC_GATE_UP_M16 = 273613568 + 5381376
+# from an ncu capture, with the SHA-256 of the GEMM kernel's sources it was taken on: the
+# line reports the traffic only while those sources are unchanged.
+TRAFFIC_GATE_UP_M16 = 273622272 + 4153344
+TRAFFIC_SOURCES_SHA256 = "4fbfb017a06a050550f19c768b6314afad41335f463fc80a5ae454613aaf2135"
+GEMM_SOURCES = ("lossless_bit_weights_gb300/csrc/w12_gemm.cu", "lossless_bit_weights_gb300/csrc/w12_internal.cuh")
+
+
+def gemm_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
+def roofline_traffic():
+    """The captured traffic of the gate/up launch if the GEMM sources are the captured ones."""
+    return TRAFFIC_GATE_UP_M16 if gemm_sources_sha256() == TRAFFIC_SOURCES_SHA256 else None
 
 
 def parse_args():
@@ -60,7 +76,7 @@ def parse_args():
     p.add_argument("--no-rows", action="store_true", help="skip the extra hot-path rows")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack rows (32 GB of W12)")
-    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead", "cert", "gdn"], default=None,
+    p.add_argument("--only", choices=[n for n, _, _ in BLOCK] + ["lmhead", "cert", "gdn", "wy"], default=None,
                    help="profiling case: repeat one matrix's GEMM (or the LM head) and print its time")
     p.add_argument("--q8", action="store_true", help="with --only: the 8-bit-view GEMM")
     return p.parse_args()
@@ -76,7 +92,7 @@ def run_only(args):
 
     torch.cuda.set_device(0)
     M = args.M
-    if args.only == "gdn":
+    if args.only in ("gdn", "wy"):
         # path verify of a 32-node tree and the commit of four accepted nodes on one
         # gated-delta-rule layer of 32 heads of 128 x 128 state
         nn, Hg, dg = 32, 32, 128
@@ -108,6 +124,9 @@ def run_only(args):
         pl = torch.tensor([int((pn > 0).sum())], dtype=torch.int32, device="cuda")
 
         def step():
+            if args.only == "wy":
+                w12.gdn_wy_verify(S, q, k, v, al, be, par, O=O, status=st)
+                return
             w12.gdn_path_verify(S, q, k, v, al, be, par, O=O, status=st)
             w12.gdn_commit(S, k, v, al, be, pl, pn, status=st)
 
@@ -120,7 +139,7 @@ def run_only(args):
             step()
         b.record()
         torch.cuda.synchronize()
-        print(json.dumps({"only": "gdn", "us_per_layer": 1e3 * a.elapsed_time(b) / args.steps,
+        print(json.dumps({"only": args.only, "us_per_layer": 1e3 * a.elapsed_time(b) / args.steps,
                           "status": int(st.item())}), flush=True)
         return
     if args.only == "cert":
@@ -520,7 +539,7 @@ def run_w12(args, world, rank, local):
                        "us_per_layer": 1e3 * elapsed_ms / K, "parallelism": f"replicas x{world}",
                        "l2": "no flush: 506 MB of W12 per step, larger than the 129 MB L2"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": TRAFFIC_GATE_UP_M16, "peak_kind": hbm_kind,
+                         "traffic": roofline_traffic(), "peak_kind": hbm_kind,
                          "kernel": "k_gemm_tc<NT=16,Q8=0,EPI=store>, gate/up launch (34816x5120, M=16)",
                          "algorithmic_bytes": gate_bytes, "launch_us": 1e3 * gate_ms,
                          "timing": "gate/up alone, back to back, CUDA events around the loop",
