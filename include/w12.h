@@ -408,9 +408,13 @@ W12_API int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* 
  * gamma_t S0 + sum_{j on path(t)} (gamma_t/gamma_j) d_j k_j^T (gamma: product of
  * alpha along the path), whose pseudo-values d_j solve a triangular system over
  * the tree; the state enters only through S0 k_t and S0 q_t, so every node is
- * computed once instead of once per path that reaches it.  dk = 64 or 128,
- * n in 1..64, S0 16-byte aligned; other arguments, errors and *status as for
- * gdn_path_verify. */
+ * computed once instead of once per path that reaches it.  Those products run on
+ * the tensor core as bf16 MMAs with fp32 accumulation over the float state split
+ * exactly into three bf16 pieces (gdn_split3's split), so every product of a state
+ * element and a k or q element is exact.  One CTA per (head, 128 state rows).
+ * dk = 64 or 128, n in 1..64, S0 16-byte aligned; other arguments, errors and
+ * *status as for gdn_path_verify; a device wait that runs out (about a second)
+ * sets bit 2 of *status. */
 W12_API int gdn_wy_verify(const float* S0, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                           const float* alpha, const float* beta, const int32_t* parent, int64_t n, int64_t H,
                           int64_t dk, int64_t dv, float* O, int32_t* status, void* stream);
