@@ -459,7 +459,8 @@ struct WyPlan {
   static constexpr int kBar = kPar + kWyMaxNodes * 4;      // staging barrier, MMA barrier
   static constexpr int kTmem = kBar + 16;
   static constexpr int kFlag = kTmem + 4;
-  static constexpr int kBytes = kFlag + 12;
+  static constexpr int kVs = kFlag + 12;                   // v of the CTA's rows, bf16 [node][row]
+  static constexpr int kBytes = kVs + kWyMaxNodes * kWyRows * 2;
   static_assert(kA + 3 * kWyMaxNodes * kWyRows * 4 <= kG, "per-row values overlap the tables");
   static_assert(kBytes <= 227 * 1024, "shared memory plan too large");
 };
@@ -506,50 +507,62 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     for (uint32_t off = 0; off < bytes; off += 16384u)
       bulk_g2s(sbase + P::kStage + off, src + off, bytes - off < 16384u ? bytes - off : 16384u, bar_stage, pol);
   }
-  // rows past dv read as zero (their lanes are never stored)
-  for (int e = rows * DK + tid; e < kWyRows * DK; e += kWyThreads) reinterpret_cast<float*>(sm + P::kStage)[e] = 0.f;
-  for (int t = tid; t < n; t += kWyThreads) {
-    par[t] = parent[t];
-    alp[t] = alpha[(int64_t)t * H + h];
-    bet[t] = beta[(int64_t)t * H + h];
-  }
-  // node tiles: rows 0..n16-1 hold k_t, rows n16..2*n16-1 q_t, the rest zero
-  for (int u = tid; u < KB * kWyRows * 8; u += kWyThreads) {
-    const int kb = u / (kWyRows * 8), R = (u / 8) % kWyRows, c8 = u & 7;
-    const uint16_t* src = nullptr;
-    if (R < n16) {
-      if (R < n) src = k + ((int64_t)R * H + h) * DK;
-    } else if (R < 2 * n16 && R - n16 < n) {
-      src = q + ((int64_t)(R - n16) * H + h) * DK;
+  // Warps 0-3 stage v of their state rows for every node; warps 4-5 read the tree and build
+  // each node's path mask and gamma; warps 6-15 zero the rows past dv and fill the node
+  // tiles.  The state rows land meanwhile.
+  uint16_t* vs = reinterpret_cast<uint16_t*>(sm + P::kVs);
+  if (warp < 4) {
+    const int R = tid;
+#pragma unroll 8
+    for (int t = 0; t < n; ++t) vs[t * kWyRows + R] = R < rows ? v[((int64_t)t * H + h) * dv + r0 + R] : (uint16_t)0;
+  } else if (warp < 6) {
+    // ---- the tree: parents checked, each node's path as a mask, gamma (root side first:
+    // a parent's index is below its child's, so rising bit order walks the path from the root)
+    const int t = tid - 128;
+    if (t < n) {
+      par[t] = parent[t];
+      alp[t] = alpha[(int64_t)t * H + h];
+      bet[t] = beta[(int64_t)t * H + h];
     }
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (src) {
-      src += kb * 64 + c8 * 8;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = pack_bf16(src[2 * i], src[2 * i + 1]);
-    }
-    sts128(sbase + P::kNodes + kb * kWyTile + R * 128 + ((c8 ^ (R & 7)) << 4), w[0], w[1], w[2], w[3]);
-  }
-  __syncthreads();
-  // ---- the tree: parents checked, each node's path as a mask, gamma (root side first: a
-  // parent's index is below its child's, so rising bit order walks the path from the root)
-  if (tid < n) {
-    const int t = tid;
-    bool ok = t == 0 ? par[0] == -1 : (par[t] >= 0 && par[t] < t);
-    unsigned long long m = 0ull;
-    if (ok)
-      for (int j = t; j > 0; j = par[j]) {
-        if (par[j] < 0 || par[j] >= j) {  // an ancestor's bad parent (also flagged by that node)
-          ok = false;
-          break;
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // warps 4 and 5
+    if (t < n) {
+      bool ok = t == 0 ? par[0] == -1 : (par[t] >= 0 && par[t] < t);
+      unsigned long long m = 0ull;
+      if (ok)
+        for (int j = t; j > 0; j = par[j]) {
+          if (par[j] < 0 || par[j] >= j) {  // an ancestor's bad parent (also flagged by that node)
+            ok = false;
+            break;
+          }
+          m |= 1ull << j;
         }
-        m |= 1ull << j;
+      if (!ok) atomicOr(flag, 1);
+      pmask[t] = m;
+      float g = 1.f;
+      for (unsigned long long r = m; r; r &= r - 1) g = alp[__ffsll((long long)r) - 1] * g;
+      gam[t] = g;
+    }
+  } else {
+    const int w6 = tid - 192, nw6 = kWyThreads - 192;
+    // rows past dv read as zero (their lanes are never stored)
+    for (int e = rows * DK + w6; e < kWyRows * DK; e += nw6) reinterpret_cast<float*>(sm + P::kStage)[e] = 0.f;
+    // node tiles: rows 0..n16-1 hold k_t, rows n16..2*n16-1 q_t, the rest zero
+    for (int u = w6; u < KB * kWyRows * 8; u += nw6) {
+      const int kb = u / (kWyRows * 8), R = (u / 8) % kWyRows, c8 = u & 7;
+      const uint16_t* src = nullptr;
+      if (R < n16) {
+        if (R < n) src = k + ((int64_t)R * H + h) * DK;
+      } else if (R < 2 * n16 && R - n16 < n) {
+        src = q + ((int64_t)(R - n16) * H + h) * DK;
       }
-    if (!ok) atomicOr(flag, 1);
-    pmask[t] = m;
-    float g = 1.f;
-    for (unsigned long long r = m; r; r &= r - 1) g = alp[__ffsll((long long)r) - 1] * g;
-    gam[t] = g;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (src) {
+        src += kb * 64 + c8 * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = pack_bf16(src[2 * i], src[2 * i + 1]);
+      }
+      sts128(sbase + P::kNodes + kb * kWyTile + R * 128 + ((c8 ^ (R & 7)) << 4), w[0], w[1], w[2], w[3]);
+    }
   }
   const bool landed = mbar_wait_bounded(bar_stage, 0u);
   if (!landed) atomicOr(flag, 4);
@@ -613,14 +626,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     }
     umma_commit(bar_mma);
   }
-  // v of this thread's state row for every node, loaded while the MMAs run (warps 0-3)
   const int Rw = (warp & 3) * 32 + lane;
-  float vr[kWyMaxNodes];
-  if (warp < 4) {
-#pragma unroll
-    for (int c = 0; c < kWyMaxNodes; ++c)
-      vr[c] = (c < n && Rw < rows) ? bf16v(v[((int64_t)c * H + h) * dv + r0 + Rw]) : 0.f;
-  }
   const bool done = mbar_wait_bounded(bar_mma, 0u);
   tc_fence_after();
   if (!done) atomicOr(flag, 4);
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = c0 + i;
-          if (c < n) A_s[c * kWyRows + Rw] = vr[c] - gam[c] * val[i];
+          if (c < n) A_s[c * kWyRows + Rw] = bf16v(vs[c * kWyRows + Rw]) - gam[c] * val[i];
         }
       }
     }
