@@ -836,8 +836,9 @@ struct LaunchShape {
 LaunchShape launch_shape(int64_t M, int64_t N, int sms) {
   const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 192 ? 192 : 256;
   if (nt <= 32) return {nt, kModeOwn, 2};
-  // row-block pairs: on matrices with a row block per SM or more, up to 128 tokens
-  const bool pair = nt <= 128 && row_blocks(N) >= sms;
+  // row-block pairs: on matrices with a row block per SM or more, up to 192 tokens (at 256
+  // a pipeline's record ring would drop to three stages)
+  const bool pair = nt <= 192 && row_blocks(N) >= sms;
   return {nt, pair ? kModePair : kModeOne, 1};
 }
 
@@ -945,7 +946,8 @@ int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, 
     case 64: return pair ? launch_tc<64, Q8, kModePair, EPI>(map, a, s) : launch_tc<64, Q8, kModeOne, EPI>(map, a, s);
     case 128:
       return pair ? launch_tc<128, Q8, kModePair, EPI>(map, a, s) : launch_tc<128, Q8, kModeOne, EPI>(map, a, s);
-    case 192: return launch_tc<192, Q8, kModeOne, EPI>(map, a, s);
+    case 192:
+      return pair ? launch_tc<192, Q8, kModePair, EPI>(map, a, s) : launch_tc<192, Q8, kModeOne, EPI>(map, a, s);
     default: return launch_tc<256, Q8, kModeOne, EPI>(map, a, s);
   }
 }
