@@ -31,7 +31,7 @@ def w12():
     return m
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 5120, 5120), (192, 2048, 5120), (64, 20480, 1024)])
+@pytest.mark.parametrize("M,N,K", [(16, 5120, 5120), (192, 2048, 5120), (64, 20480, 1024), (192, 20480, 1024)])
 def test_wait_timeout_is_reported_and_the_workspace_recovers(w12, M, N, K):
     layer = 11
     Wd = device_weights(0, layer, M, N, K)
