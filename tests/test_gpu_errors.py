@@ -3,8 +3,10 @@
 - A wait that runs out: with the GEMM kernels' wait bound lowered far below a unit's
   latency (w12_set_wait_limit), every CTA gives up early, leaves nothing in flight and
   frees its tensor memory; w12_workspace_status then reports W12_ERR_TIMEOUT and clears
-  the workspace, and the next call on the same workspace gives the full result.  No GPU
-  fault is involved: the kernels return normally.
+  the workspace, and the next call on the same workspace gives the full result, in every
+  launch mode (two pipelines with their own ranges at 16 tokens, one pipeline at 192 tokens
+  on a short matrix, row-block pairs at 64 and 192 tokens on tall ones).  No GPU fault is
+  involved: the kernels return normally.
 - A damaged escape index: w12_validate reports W12_ERR_BOUNDS for index arrays corrupted
   on the host (copies of a valid matrix's); such a matrix is never given to a GEMM.
 """
