@@ -48,8 +48,8 @@ METRIC = "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (34816x5120, M=16)
 # from an ncu capture, with the SHA-256 of the GEMM kernel's sources it was taken on: the
 # line reports the traffic only while those sources are unchanged.
-TRAFFIC_GATE_UP_M16 = 273626368 + 4039936
-TRAFFIC_SOURCES_SHA256 = "6d7cb3b8519b088736593827137b9c1069e6aec98a6d5be52fe3c7466e82445c"
+TRAFFIC_GATE_UP_M16 = 273629184 + 5419520
+TRAFFIC_SOURCES_SHA256 = "82d6745b3e718293eb3fa141cea55b57eb154c191c761d4a25315badd064ee6f"
 GEMM_SOURCES = ("lossless_bit_weights_gb300/csrc/w12_gemm.cu", "lossless_bit_weights_gb300/csrc/w12_internal.cuh")
 
 
@@ -540,7 +540,7 @@ def run_w12(args, world, rank, local):
                        "l2": "no flush: 506 MB of W12 per step, larger than the 129 MB L2"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": roofline_traffic(), "peak_kind": hbm_kind,
-                         "kernel": "k_gemm_tc<NT=16,Q8=0,EPI=store>, gate/up launch (34816x5120, M=16)",
+                         "kernel": "k_gemm_tc<NT=16,Q8=0,mode=pair,EPI=store>, gate/up launch (34816x5120, M=16)",
                          "algorithmic_bytes": gate_bytes, "launch_us": 1e3 * gate_ms,
                          "timing": "gate/up alone, back to back, CUDA events around the loop",
                          "block_achieved": achieved_block, "block_frac": achieved_block / hbm,

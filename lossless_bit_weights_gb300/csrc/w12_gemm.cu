@@ -114,17 +114,19 @@ constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 blo
 
 // Launch modes.  A pipeline is a producer warp, two decode groups, an MMA issuer and an x
 // warp, with its own shared memory, barriers and TMEM columns.
-//  kModeOwn  (NT <= 32): two pipelines per CTA, one CTA per SM, each pipeline with its own
-//            unit range (units = row block x 64 columns).  As two CTAs on an SM, the older
-//            one's warps were favoured by the scheduler and it finished its equal share
-//            ~6 us sooner on gate/up (a launch ends with the slower one); as two pipelines
-//            of one CTA they finish together on average.
-//  kModeOne  (NT >= 64): one pipeline per CTA; its x chunks are large.
-//  kModePair (NT >= 64): two pipelines share one range of row-block pairs x 64 columns,
-//            pipeline p on row block 2*pair + p, and one x warp and ring (each stage freed
-//            by both MMA issuers).  Twice the decode warps of kModeOne per SM, at the cost
-//            of stream-K splits over twice as many CTAs per (longer) row: it pays on tall
-//            matrices only.
+//  kModeOwn  (NT <= 32 on matrices with fewer row blocks than SMs): two pipelines per CTA,
+//            one CTA per SM, each pipeline with its own unit range (units = row block x 64
+//            columns).  As two CTAs on an SM, the older one's warps were favoured by the
+//            scheduler and it finished its equal share ~6 us sooner on gate/up (a launch
+//            ends with the slower one); as two pipelines of one CTA they finish together.
+//  kModeOne  (NT >= 64 on short matrices, and 256): one pipeline per CTA; its x chunks are
+//            large.
+//  kModePair (up to 192 tokens on matrices with a row block per SM or more): two pipelines
+//            share one range of row-block pairs x 64 columns, pipeline p on row block
+//            2*pair + p, and one x warp and ring (each stage freed by both MMA issuers).
+//            Against kModeOne: twice the decode warps per SM; against kModeOwn: one x
+//            stream for both pipelines and deeper record rings.  Stream-K splits run over
+//            twice as many CTAs per (longer) row, so it pays on tall matrices only.
 enum { kModeOwn = 0, kModeOne = 1, kModePair = 2 };
 
 template <int NT, bool Q8, int MODE>
@@ -174,7 +176,7 @@ struct TcPlan {
   static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
   static_assert(kABufs >= kGroups, "an A buffer per decode group at least");
   static_assert(kCtaBytes <= 227 * 1024, "shared memory plan too large");
-  static_assert((MODE == kModeOwn) == (NT <= 32), "launch mode does not fit the token tile");
+  static_assert(MODE != kModeOwn || NT <= 32, "launch mode does not fit the token tile");
   static_assert(kPipes * kTmemCols <= 512, "tensor memory plan too large");
 };
 
@@ -835,7 +837,9 @@ struct LaunchShape {
 };
 LaunchShape launch_shape(int64_t M, int64_t N, int sms) {
   const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 192 ? 192 : 256;
-  if (nt <= 32) return {nt, kModeOwn, 2};
+  // up to 32 tokens: row-block pairs on tall matrices (a row block per SM or more), else two
+  // pipelines with their own ranges
+  if (nt <= 32) return row_blocks(N) >= sms ? LaunchShape{nt, kModePair, 1} : LaunchShape{nt, kModeOwn, 2};
   // row-block pairs: on matrices with a row block per SM or more, up to 192 tokens (at 256
   // a pipeline's record ring would drop to three stages)
   const bool pair = nt <= 192 && row_blocks(N) >= sms;
@@ -941,8 +945,8 @@ template <bool Q8, int EPI>
 int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
   const bool pair = ls.mode == kModePair;
   switch (ls.nt) {
-    case 16: return launch_tc<16, Q8, kModeOwn, EPI>(map, a, s);
-    case 32: return launch_tc<32, Q8, kModeOwn, EPI>(map, a, s);
+    case 16: return pair ? launch_tc<16, Q8, kModePair, EPI>(map, a, s) : launch_tc<16, Q8, kModeOwn, EPI>(map, a, s);
+    case 32: return pair ? launch_tc<32, Q8, kModePair, EPI>(map, a, s) : launch_tc<32, Q8, kModeOwn, EPI>(map, a, s);
     case 64: return pair ? launch_tc<64, Q8, kModePair, EPI>(map, a, s) : launch_tc<64, Q8, kModeOne, EPI>(map, a, s);
     case 128:
       return pair ? launch_tc<128, Q8, kModePair, EPI>(map, a, s) : launch_tc<128, Q8, kModeOne, EPI>(map, a, s);
