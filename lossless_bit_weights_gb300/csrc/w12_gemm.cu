@@ -148,8 +148,9 @@ struct TcPlan {
   static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : 2;
   // A buffers (decoded 128x64 tiles) in rotation over the pipeline's units: with more than
   // one per decode group, a group stores a unit while the MMA of the unit before its previous
-  // one may still run
-  static constexpr int kABufs = MODE == kModeOwn ? 3 : MODE == kModeOne ? 4 : 2;
+  // one may still run.  At 16 tokens with own ranges a fifth record stage measured better
+  // than a third A buffer.
+  static constexpr int kABufs = MODE == kModeOwn ? (NT <= 16 ? 2 : 3) : MODE == kModeOne ? 4 : 2;
   // shared x region (wide): x stages, then x_full[SX] x_empty[SX]
   static constexpr int kXRegion = kWide ? (kXStages * kX + 2 * kXStages * 8 + 1023) / 1024 * 1024 : 0;
   static constexpr int kOffXBar = kXStages * kX;
