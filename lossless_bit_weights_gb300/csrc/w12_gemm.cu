@@ -145,7 +145,9 @@ struct TcPlan {
   // 22-warp CTA puts six on one, so 80 registers a thread is the most that launches.
   static constexpr int kBoundThreads = kPipes == 1 ? kCtaThreads : kCtaThreads > 704 ? kCtaThreads : 704;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
-  static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : 2;
+  // x stages: at 192 tokens with row-block pairs a third 24 KB stage (shared by both
+  // pipelines) measured better than a fourth record stage per pipeline
+  static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : (MODE == kModePair && NT == 192) ? 3 : 2;
   // A buffers (decoded 128x64 tiles) in rotation over the pipeline's units: with more than
   // one per decode group, a group stores a unit while the MMA of the unit before its previous
   // one may still run.  At 16 tokens with own ranges a fifth record stage measured better
