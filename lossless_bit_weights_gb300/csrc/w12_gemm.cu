@@ -727,7 +727,66 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
             bail = true;
             break;
           }
-          if (emit) {
+          // At the pipeline's last unit every record stage and A buffer has been consumed
+          // (the accumulator barrier follows every MMA, and each MMA follows its unit's
+          // decode): each warp of the group then takes a quarter of that space and fetches
+          // the parts' slots with bulk copies, all in flight at once, where the fallback
+          // below waits for one L2 round trip per slot.  Both add the slots in part order.
+          constexpr int kPiece = 16 * 32 * 4;  // 16 token columns of one warp's slot
+          constexpr int kQuarter = ((P::kOffBar - P::kOffA) / 4) & ~(kPiece - 1);
+          const int per = kQuarter / (kPiece * (int)ncov);  // column chunks per batch
+          if (emit && j == nunp - 1 && per >= 1) {
+            if (tl == 0 && lane == 0) a.counters[rb] = 0u;
+            const uint32_t sc = sbase + P::kOffA + tl * kQuarter;
+            const uint32_t fb = smem_u32(misc + 4 + 2 * tl);
+            if (lane == 0) {
+              mbar_init(fb, 1);
+              mbar_init_fence();
+              fence_proxy_async_smem();    // earlier generic accesses of the space -> the copies
+              fence_proxy_async_global();  // the other parts' slots, acquired above -> the copies
+            }
+            __syncwarp();
+            const uint64_t pol_s = policy_evict_first();
+            uint32_t fph = 0;
+#pragma unroll 1
+            for (int c = 0; c < NT / 16 && !bail; c += per) {
+              const int nb = min(per, NT / 16 - c);
+              if (lane == 0) {
+                mbar_arrive_expect_tx(fb, (uint32_t)(nb * ncov * kPiece));
+                for (int cc = 0; cc < nb; ++cc)
+                  for (int64_t jj = 0; jj < ncov; ++jj)
+                    bulk_g2s(sc + (uint32_t)((cc * ncov + jj) * kPiece),
+                             a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot + (c + cc) * 16 * 32, kPiece,
+                             fb, pol_s);
+              }
+              if (!warp_wait(fb, fph)) {
+                if (lane == 0) mbar_wait_bounded(fb, fph);  // copies in flight land before the CTA leaves
+                bail = true;
+                break;
+              }
+              fph ^= 1u;
+#pragma unroll 1
+              for (int cc = 0; cc < nb; ++cc) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                for (int64_t jj = 0; jj < ncov; ++jj) {
+                  const uint32_t pc = sc + (uint32_t)((cc * ncov + jj) * kPiece) + (uint32_t)lane * 16u;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const uint4 q4 = lds128(pc + (uint32_t)i * 512u);
+                    v[4 * i] += __uint_as_float(q4.x);
+                    v[4 * i + 1] += __uint_as_float(q4.y);
+                    v[4 * i + 2] += __uint_as_float(q4.z);
+                    v[4 * i + 3] += __uint_as_float(q4.w);
+                  }
+                }
+                emit_cols<EPI>(a, rt, lane, (c + cc) * 16, v);
+              }
+              __syncwarp();  // every lane has read the batch before the next one lands
+            }
+            if (bail) break;
+          } else if (emit) {
             if (tl == 0 && lane == 0) a.counters[rb] = 0u;
 #pragma unroll 1
             for (int c0 = 0; c0 < NT; c0 += 16) {
