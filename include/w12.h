@@ -367,6 +367,8 @@ W12_API size_t w12_cert_head_workspace_size(int64_t M, int64_t V, int64_t K);
  * the row's largest approximate logit minus bound, rounded outward), and the
  * candidates' logits are recomputed from `exact`, the W12 form of the same head
  * (exact bf16 products, a float-pair sum whose error is near 2^-48 sum|x*w|).  ncand[m] (may be NULL) receives the candidate count.
+ * The approximate logits are never stored: the INT8 GEMM's epilogue keeps each
+ * row's threshold and a superset of its candidates, which the recompute filters.
  * Workspace >= w12_cert_head_workspace_size(M, V, K) bytes, first
  * w12_gemm_counter_bytes(V) bytes zero before first use (as for w12_gemm).
  * Errors: W12_ERR_INVALID_ARG, W12_ERR_SHAPE (shapes of H and exact differ,

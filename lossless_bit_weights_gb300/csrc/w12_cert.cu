@@ -23,12 +23,12 @@
 namespace w12 {
 
 int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float* scale, int64_t V, int64_t K,
-                 float* y, void* ws, size_t ws_bytes, cudaStream_t s, const char* fn);
+                 const float* nx, const float* cb, uint32_t* thr_key, uint32_t* sup_count, uint2* sup,
+                 int64_t ldsup, void* ws, size_t ws_bytes, cudaStream_t s, const char* fn);
 
 namespace {
 
 constexpr int kExactBlocks = 256;  // blocks per row of the exact recompute
-constexpr int kThrBlocks = 64;     // blocks per row of the threshold
 constexpr int kExactWarps = 10;    // 10 x 8 chunks: K = 5120 in one round
 
 inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -106,8 +106,14 @@ __global__ void __launch_bounds__(256) k_i8_encode(const uint16_t* __restrict__ 
 }
 
 // nx[m] >= ||x_m||: every square and every addition rounds
-// up, so the sum (and its square root, rounded up) bound the norm from above.
-__global__ void __launch_bounds__(256) k_rownorm(const uint16_t* __restrict__ x, int64_t K, float* __restrict__ nx) {
+// up, so the sum (and its square root, rounded up) bound the norm from above.  Also zeroes
+// the row's threshold key and counters for the GEMM's epilogue and the exact recompute.
+__global__ void __launch_bounds__(256) k_cert_prep(const uint16_t* __restrict__ x, int64_t K, float* __restrict__ nx,
+                                                   uint32_t* __restrict__ thr_key, int32_t* __restrict__ count,
+                                                   uint32_t* __restrict__ sup_count) {
+  // the GEMM that follows may start streaming its weights; it reads nothing of ours
+  // before its griddepcontrol.wait
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float shf[32];
   const uint16_t* xr = x + (int64_t)blockIdx.x * K;
   float a = 0.f;
@@ -122,42 +128,15 @@ __global__ void __launch_bounds__(256) k_rownorm(const uint16_t* __restrict__ x,
     float t = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = __fadd_ru(t, shf[w]);
     nx[blockIdx.x] = __fsqrt_ru(t);
+    thr_key[blockIdx.x] = 0u;
+    count[blockIdx.x] = 0;
+    sup_count[blockIdx.x] = 0u;
   }
 }
 
-// Order-preserving map of floats to unsigned keys (larger float, larger key; key 0 is
-// below every float), so that a maximum can be taken with atomicMax in any order.
-__device__ __forceinline__ uint32_t fkey(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+// Inverse of the GEMM epilogue's order-preserving key (larger float, larger key).
 __device__ __forceinline__ float fkey_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// thr[m] = max_v (approx[m,v] - bound[m,v]), every step rounded down; thr_key zero beforehand.
-__global__ void __launch_bounds__(1024) k_cert_thr(const float* __restrict__ lh, int64_t V, const float* __restrict__ nx,
-                                                   const float* __restrict__ cb, uint32_t* __restrict__ thr_key) {
-  __shared__ float shf[32];
-  const int64_t m = blockIdx.y;
-  const float n = nx[m];
-  float t = -INFINITY;
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < V; v += (int64_t)gridDim.x * blockDim.x)
-    t = fmaxf(t, __fsub_rd(lh[m * V + v], __fmul_ru(n, cb[v])));
-  t = block_max(t, shf);
-  if (threadIdx.x == 0) atomicMax(thr_key + m, fkey(t));
-}
-
-// Candidates: approx + bound (rounded up) >= thr.
-__global__ void __launch_bounds__(1024) k_cert_cand(const float* __restrict__ lh, int64_t V, const float* __restrict__ nx,
-                                                    const float* __restrict__ cb, const uint32_t* __restrict__ thr_key,
-                                                    int32_t* __restrict__ count, int32_t* __restrict__ cand) {
-  const int64_t m = blockIdx.y, v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= V) return;
-  if (__fadd_ru(lh[m * V + v], __fmul_ru(nx[m], cb[v])) >= fkey_inv(thr_key[m])) {
-    const int pos = atomicAdd(count + m, 1);
-    cand[m * V + pos] = (int32_t)v;
-  }
 }
 
 struct Best {
@@ -185,93 +164,120 @@ __device__ __forceinline__ bool beats(double a, int32_t ia, double b, int32_t ib
   return a > b || (a == b && ia < ib);
 }
 
-// Exact logits of the candidates from the W12 head.  Block b of row m takes candidates
-// b, b + gridDim.x, ...; its 10 warps split the candidate's column chunks: lane 4*c8 + t
-// of warp w decodes the 16 columns 16t.. of chunks w*8 + c8 + 80i (the same decode as
-// the GEMM) and patches the channel's escapes in them.  A product of two bf16 values is
-// exact in float; the sum is a float pair (TwoSum), whose error is near 2^-48 of
-// sum|x*w|, far inside the argmax's tie tolerance and on the full-rate float pipe
-// (float64 runs at a small fraction of it on this GPU).
+// Exact logits of the candidates from the W12 head.  Block b of row m takes the superset
+// entries b, b + gridDim.x, ... (one per thread in each round), keeps those whose upper
+// bound reaches the row's final threshold (the candidates) in a shared list, and computes
+// each candidate with the whole block: lane 4*c8 + t of warp w decodes the 16 columns
+// 16t.. of chunks w*8 + c8 + 80i (the same decode as the GEMM) and patches the channel's
+// escapes in them.  A product of two bf16 values is exact in float; the sum is a float
+// pair (TwoSum), whose error is near 2^-48 of sum|x*w|, far inside the argmax's tie
+// tolerance and on the full-rate float pipe (float64 runs at a small fraction of it on
+// this GPU).  count[m] (zero beforehand) receives the number of candidates.
 __global__ void __launch_bounds__(kExactWarps * 32)
     k_cert_exact(const uint16_t* __restrict__ x, int64_t K, int64_t KC, const uint8_t* __restrict__ hi,
                  const uint8_t* __restrict__ lo, const uint8_t* __restrict__ base, const uint32_t* __restrict__ tile_ptr,
-                 const uint32_t* __restrict__ esc, const int32_t* __restrict__ count, const int32_t* __restrict__ cand,
-                 int64_t V, DecodeMul mul, Best* __restrict__ part) {
+                 const uint32_t* __restrict__ esc, const uint32_t* __restrict__ thr_key,
+                 const uint32_t* __restrict__ sup_count, const uint2* __restrict__ sup, int64_t ldsup,
+                 int32_t* __restrict__ count, DecodeMul mul, Best* __restrict__ part) {
+  // the final merge may launch now; everything here waits for the INT8 GEMM to complete
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float shh[kExactWarps], shl[kExactWarps];
+  __shared__ int32_t sh_cand[kExactWarps * 32];
+  __shared__ int sh_n;
   const int64_t m = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c8 = lane >> 2, t = lane & 3;
-  const int n_c = count[m];
+  const uint32_t n_sup = min(sup_count[m], (uint32_t)ldsup);
+  const float thr = fkey_inv(thr_key[m]);
   const uint16_t* xr = x + m * K;
   Best best{0.0, -1};
-  for (int i = blockIdx.x; i < n_c; i += gridDim.x) {
-    const int64_t v = cand[m * V + i];
-    const int64_t rt = v / kTileRows;
-    const int r = (int)(v % kTileRows), q = r >> 3, g = r & 7;
-    const uint32_t bb = base[v];
-    const uint32_t base2 = (bb << 7) | (bb << 23);
-    float ah = 0.f, al = 0.f;
-    for (int64_t kc = warp * 8 + c8; kc < KC; kc += kExactWarps * 8) {
-      const int64_t tile = tile_index(rt, kc, KC);
-      const uint4 hq = *reinterpret_cast<const uint4*>(hi + tile * kHiTileBytes + q * 512 + (4 * g + t) * 16);
-      const uint2 lq = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
-      const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
-      uint32_t pr[8];
-      decode16<false>(hq, lq, base2, mul, pr);
-      uint16_t w[16];
+  int mine = 0;
+  for (uint32_t r0 = blockIdx.x; r0 < n_sup; r0 += gridDim.x * blockDim.x) {
+    if (threadIdx.x == 0) sh_n = 0;
+    __syncthreads();
+    const uint32_t e = r0 + threadIdx.x * gridDim.x;
+    if (e < n_sup) {
+      const uint2 ent = sup[m * ldsup + e];
+      if (fkey_inv(ent.y) >= thr) sh_cand[atomicAdd(&sh_n, 1)] = (int32_t)ent.x;
+    }
+    __syncthreads();
+    const int nc = sh_n;
+    mine += nc;
+    for (int i = 0; i < nc; ++i) {
+      const int64_t v = sh_cand[i];
+      const int64_t rt = v / kTileRows;
+      const int r = (int)(v % kTileRows), q = r >> 3, g = r & 7;
+      const uint32_t bb = base[v];
+      const uint32_t base2 = (bb << 7) | (bb << 23);
+      float ah = 0.f, al = 0.f;
+      for (int64_t kc = warp * 8 + c8; kc < KC; kc += kExactWarps * 8) {
+        const int64_t tile = tile_index(rt, kc, KC);
+        const uint4 hq = *reinterpret_cast<const uint4*>(hi + tile * kHiTileBytes + q * 512 + (4 * g + t) * 16);
+        const uint2 lq = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
+        const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
+        uint32_t pr[8];
+        decode16<false>(hq, lq, base2, mul, pr);
+        uint16_t w[16];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        w[2 * p] = (uint16_t)(pr[p] & 0xFFFFu);
-        w[2 * p + 1] = (uint16_t)(pr[p] >> 16);
-      }
-      // the tile's escapes, four independent loads at a time
-      for (uint32_t e = e0; e < e1; e += 4) {
-        uint32_t ent[4];
+        for (int p = 0; p < 8; ++p) {
+          w[2 * p] = (uint16_t)(pr[p] & 0xFFFFu);
+          w[2 * p + 1] = (uint16_t)(pr[p] >> 16);
+        }
+        // the tile's escapes, four independent loads at a time
+        for (uint32_t e = e0; e < e1; e += 4) {
+          uint32_t ent[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ent[u] = e + u < e1 ? esc[e + u] : 0xFFFFFFFFu;
+          for (int u = 0; u < 4; ++u) ent[u] = e + u < e1 ? esc[e + u] : 0xFFFFFFFFu;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = esc_col(ent[u]);
-          if (ent[u] != 0xFFFFFFFFu && esc_row(ent[u]) == r && (c >> 4) == t) {
+          for (int u = 0; u < 4; ++u) {
+            const int c = esc_col(ent[u]);
+            if (ent[u] != 0xFFFFFFFFu && esc_row(ent[u]) == r && (c >> 4) == t) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent[u]);
+              for (int j = 0; j < 16; ++j)
+                if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent[u]);
+            }
           }
         }
-      }
-      const int64_t k0 = kc * kTileK + 16 * t;
+        const int64_t k0 = kc * kTileK + 16 * t;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (k0 + j < K) acc2(ah, al, __fmul_rn(bf16f(xr[k0 + j]), bf16f(w[j])));
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ah, o), ol = __shfl_xor_sync(0xFFFFFFFFu, al, o);
-      acc2(ah, al, oh);
-      al = __fadd_rn(al, ol);
-    }
-    if (lane == 0) {
-      shh[warp] = ah;
-      shl[warp] = al;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float h = shh[0], l = shl[0];
-      for (int w2 = 1; w2 < kExactWarps; ++w2) {
-        acc2(h, l, shh[w2]);
-        l = __fadd_rn(l, shl[w2]);
+        for (int j = 0; j < 16; ++j)
+          if (k0 + j < K) acc2(ah, al, __fmul_rn(bf16f(xr[k0 + j]), bf16f(w[j])));
       }
-      const double acc = (double)h + (double)l;
-      if (beats(acc, (int32_t)v, best.val, best.idx)) best = Best{acc, (int32_t)v};
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xFFFFFFFFu, ah, o), ol = __shfl_xor_sync(0xFFFFFFFFu, al, o);
+        acc2(ah, al, oh);
+        al = __fadd_rn(al, ol);
+      }
+      if (lane == 0) {
+        shh[warp] = ah;
+        shl[warp] = al;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float h = shh[0], l = shl[0];
+        for (int w2 = 1; w2 < kExactWarps; ++w2) {
+          acc2(h, l, shh[w2]);
+          l = __fadd_rn(l, shl[w2]);
+        }
+        const double acc = (double)h + (double)l;
+        if (beats(acc, (int32_t)v, best.val, best.idx)) best = Best{acc, (int32_t)v};
+      }
+      __syncthreads();
     }
-    __syncthreads();
+    __syncthreads();  // every thread has read the round's count before the next round resets it
   }
-  if (threadIdx.x == 0) part[m * gridDim.x + blockIdx.x] = best;
+  if (threadIdx.x == 0) {
+    part[m * gridDim.x + blockIdx.x] = best;
+    if (mine) atomicAdd(count + m, mine);
+  }
 }
 
 // One block of 256 per row: thread i merges partials i and i + 256, then the warps and
 // the block merge in a fixed order.
 __global__ void __launch_bounds__(256) k_cert_final(const Best* __restrict__ part, const int32_t* __restrict__ count,
                                                     int32_t* __restrict__ tok, int32_t* __restrict__ ncand) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the exact recompute has completed
   __shared__ Best sh[8];
   const int64_t m = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -296,22 +302,24 @@ __global__ void __launch_bounds__(256) k_cert_final(const Best* __restrict__ par
 }
 
 struct CertWs {
-  size_t gemm, lh, nx, thr, count, cand, part, total;
+  size_t gemm, nx, thr, count, sup_count, sup, part, total;
 };
 
+// The candidate superset of a row holds at most one entry per channel: M x V entries.
 CertWs cert_ws(int64_t M, int64_t V, int64_t K) {
   CertWs L{};
   L.gemm = 0;
   size_t off = al256(w12_gemm_workspace_size(M, V, K));
-  L.lh = off;
-  off = al256(off + (size_t)M * (size_t)V * 4);
   L.nx = off;
   off = al256(off + (size_t)M * 4);
-  L.thr = off;  // thr keys, then counts: zeroed by one memset
-  L.count = off + (size_t)M * 4;
-  off = al256(off + (size_t)M * 8);
-  L.cand = off;
-  off = al256(off + (size_t)M * (size_t)V * 4);
+  L.thr = off;
+  off = al256(off + (size_t)M * 4);
+  L.count = off;
+  off = al256(off + (size_t)M * 4);
+  L.sup_count = off;
+  off = al256(off + (size_t)M * 4);
+  L.sup = off;
+  off = al256(off + (size_t)M * (size_t)V * 8);
   L.part = off;
   off = al256(off + (size_t)M * kExactBlocks * sizeof(Best));
   L.total = off;
@@ -372,26 +380,38 @@ int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, con
     return fail(W12_ERR_BUFFER_TOO_SMALL, "%s: workspace %zu bytes < %zu required", fn, ws_bytes, L.total);
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  float* lh = reinterpret_cast<float*>(w + L.lh);
   float* nx = reinterpret_cast<float*>(w + L.nx);
   uint32_t* thr = reinterpret_cast<uint32_t*>(w + L.thr);
   int32_t* count = reinterpret_cast<int32_t*>(w + L.count);
-  int32_t* cand = reinterpret_cast<int32_t*>(w + L.cand);
+  uint32_t* sup_count = reinterpret_cast<uint32_t*>(w + L.sup_count);
+  uint2* sup = reinterpret_cast<uint2*>(w + L.sup);
   Best* part = reinterpret_cast<Best*>(w + L.part);
-  // approximate logits s_v * x.q_v
-  if ((st = i8_gemm_impl(x, M, H->code, H->scale, V, K, lh, w + L.gemm, L.lh, s, fn))) return st;
-  k_rownorm<<<(unsigned)M, 256, 0, s>>>(x, K, nx);
+  // row norms; zero thresholds and counters
+  k_cert_prep<<<(unsigned)M, 256, 0, s>>>(x, K, nx, thr, count, sup_count);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: row norms");
-  W12_CUDA_TRY(cudaMemsetAsync(thr, 0, (size_t)M * 8, s));
-  k_cert_thr<<<dim3(kThrBlocks, (unsigned)M), 1024, 0, s>>>(lh, V, nx, H->cbound, thr);
-  W12_LAUNCH_CHECK("w12_cert_head_argmax: threshold");
-  k_cert_cand<<<dim3((unsigned)((V + 1023) / 1024), (unsigned)M), 1024, 0, s>>>(lh, V, nx, H->cbound, thr, count, cand);
-  W12_LAUNCH_CHECK("w12_cert_head_argmax: candidates");
-  k_cert_exact<<<dim3(kExactBlocks, (unsigned)M), kExactWarps * 32, 0, s>>>(
-      x, K, KC, exact->hi, exact->lo, exact->base, exact->esc_tile_ptr, exact->esc, count, cand, V, W12_DECODE_MUL,
-      part);
+  // approximate logits s_v * x.q_v -> thresholds and the candidate superset
+  if ((st = i8_gemm_impl(x, M, H->code, H->scale, V, K, nx, H->cbound, thr, sup_count, sup, V, w + L.gemm, L.nx, s,
+                         fn)))
+    return st;
+  // the two kernels after the GEMM start early (programmatic dependent launch) and wait for
+  // their predecessor's grid before reading its results
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kExactBlocks, (unsigned)M);
+  cfg.blockDim = dim3(kExactWarps * 32);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_cert_exact, x, K, KC, (const uint8_t*)exact->hi, (const uint8_t*)exact->lo,
+                                  (const uint8_t*)exact->base, (const uint32_t*)exact->esc_tile_ptr,
+                                  (const uint32_t*)exact->esc, (const uint32_t*)thr, (const uint32_t*)sup_count,
+                                  (const uint2*)sup, (int64_t)V, count, W12_DECODE_MUL, part));
   W12_LAUNCH_CHECK("w12_cert_head_argmax: exact logits");
-  k_cert_final<<<(unsigned)M, 256, 0, s>>>(part, count, tok, ncand);
+  cfg.gridDim = dim3((unsigned)M);
+  cfg.blockDim = dim3(256);
+  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_cert_final, (const Best*)part, (const int32_t*)count, tok, ncand));
   W12_LAUNCH_CHECK("w12_cert_head_argmax: final");
   return W12_OK;
 }

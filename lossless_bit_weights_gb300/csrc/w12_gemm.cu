@@ -54,8 +54,27 @@ constexpr uint32_t kErrBounds = 2u;   // an escape offset lay outside the escape
 __constant__ long long c_wait_limit = kWaitCycles;
 
 // EPI_I8: the weights are INT8 codes (sign<<7 | |q|, in the hi-plane layout; no lo plane,
-// window bases or escapes) and the output is scale[n] * acc.
+// window bases or escapes); the approximate logit of token m and channel n is
+// scale[n] * acc, and the epilogue feeds the certified argmax (CertEpi) instead of
+// storing it.
 enum Epi { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_I8 = 2 };
+
+// The certified argmax's use of the approximate logits a (EPI_I8).  With the bound
+// b = nx[m] * cb[n] (rounded up), the threshold of token m is max_n (a - b) rounded down,
+// kept as an order-preserving key in thr_key[m] (atomicMax; zero beforehand); a channel is
+// a candidate when a + b (rounded up) reaches the final threshold.  Each warp appends to
+// sup[m*ldsup ..] (count in sup_count[m], zero beforehand) every channel whose a + b reaches
+// the largest threshold known to it (its own channels' and the running value): a superset
+// of the candidates, since every known value is at most the final threshold.  An entry is
+// (channel, key of a + b).
+struct CertEpi {
+  const float* nx;
+  const float* cb;
+  uint32_t* thr_key;
+  uint32_t* sup_count;
+  uint2* sup;
+  int64_t ldsup;
+};
 
 struct GemmArgs {
   const uint8_t* hi;
@@ -79,7 +98,18 @@ struct GemmArgs {
   int64_t RB;  // row blocks of the matrix
   const float* scale;  // EPI_I8: per-channel scale
   uint32_t n_esc;      // escape entries; escape offsets are clamped to it
+  CertEpi cert;        // EPI_I8
 };
+
+// Order-preserving map of floats to unsigned keys (larger float, larger key; key 0 is
+// below every float).
+__device__ __forceinline__ uint32_t order_key32(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key32_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 __device__ __forceinline__ int64_t cta_of_unit(int64_t i, int64_t G, int64_t T) { return ((i + 1) * G - 1) / T; }
 
@@ -264,11 +294,41 @@ __device__ __forceinline__ void emit_cols(const GemmArgs& a, int64_t rt, int lan
       if (tok < a.M && n < a.N) a.y[(int64_t)tok * a.ldy + n] = v[i];
     }
   } else if (EPI == EPI_I8) {
-    const float sc = n < a.N ? a.scale[n] : 0.f;
+    const bool ch = n < a.N;
+    const float sc = ch ? a.scale[n] : 0.f, cbn = ch ? a.cert.cb[n] : 0.f;
+    // lane i < 16: token c0 + i's row norm and the running threshold (any stale value is a
+    // lower bound of the final one)
+    const int tl16 = c0 + (lane & 15);
+    const bool tv = lane < 16 && tl16 < a.M;
+    const int64_t mrow = (int64_t)a.tok0 + tl16;
+    const float nxl = tv ? a.cert.nx[mrow] : 0.f;
+    const uint32_t runl = tv ? *reinterpret_cast<const volatile uint32_t*>(a.cert.thr_key + mrow) : 0u;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = c0 + i;
-      if (tok < a.M && n < a.N) a.y[(int64_t)tok * a.ldy + n] = v[i] * sc;
+      if (tok >= a.M) break;  // warp-uniform
+      const float nt = __shfl_sync(0xFFFFFFFFu, nxl, i);
+      const uint32_t run = __shfl_sync(0xFFFFFFFFu, runl, i);
+      const float lh = v[i] * sc;
+      const float bnd = __fmul_ru(nt, cbn);
+      const float up = __fadd_ru(lh, bnd);
+      const float down = __fsub_rd(lh, bnd);
+      uint32_t lo = (ch && down == down) ? order_key32(down) : 0u;  // a NaN is never the threshold
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lo = max(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+      const int64_t m = (int64_t)a.tok0 + tok;
+      if (lane == 0 && lo > run) atomicMax(a.cert.thr_key + m, lo);
+      const uint32_t known = max(lo, run);
+      const bool keep = ch && known != 0u && up >= order_key32_inv(known);
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+      if (bal) {
+        uint32_t b0 = 0u;
+        if (lane == 0) b0 = atomicAdd(a.cert.sup_count + m, (uint32_t)__popc(bal));
+        b0 = __shfl_sync(0xFFFFFFFFu, b0, 0);
+        if (keep)
+          a.cert.sup[m * a.cert.ldsup + b0 + (uint32_t)__popc(bal & ((1u << lane) - 1u))] =
+              make_uint2((uint32_t)n, order_key32(up));
+      }
     }
   } else {
 #pragma unroll
@@ -1025,7 +1085,7 @@ int check_gemm_args(const uint16_t* x, int64_t M, const w12_matrix* A, const flo
   // i8: A->hi holds INT8 codes (the caller has checked A's shape and pointers)
   int st = i8 ? W12_OK : check_matrix(A, !q8, fn);
   if (st) return st;
-  if (!x || (!argmax && !y) || (argmax && !tok)) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!x || (!argmax && !i8 && !y) || (argmax && !tok)) return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 1 || M > (1 << 20)) return fail(W12_ERR_SHAPE, "%s: M=%lld out of range (1..2^20)", fn, (long long)M);
   if ((((uintptr_t)A->hi | (uintptr_t)A->lo | (uintptr_t)A->esc) & 15u) != 0)
     return fail(W12_ERR_INVALID_ARG, "%s: hi, lo and esc must be 16-byte aligned", fn);
@@ -1037,7 +1097,8 @@ int check_gemm_args(const uint16_t* x, int64_t M, const w12_matrix* A, const flo
 }
 
 int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_t* tok, bool q8, bool argmax,
-             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn, const float* i8_scale = nullptr) {
+             void* ws, size_t ws_bytes, cudaStream_t s, const char* fn, const float* i8_scale = nullptr,
+             const CertEpi* cert = nullptr) {
   int st = check_gemm_args(x, M, A, y, tok, q8, argmax, i8_scale != nullptr, fn);
   if (st) return st;
   if (!ws) return fail(W12_ERR_INVALID_ARG, "%s: null workspace", fn);
@@ -1083,6 +1144,7 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.mul = W12_DECODE_MUL;
   a.scale = i8_scale;
   a.n_esc = i8_scale ? 0u : (uint32_t)A->n_esc;
+  if (cert) a.cert = *cert;
   CUtensorMap map;
   if ((st = make_x_map(&map, xs, M, A->K, ldx, ls.nt))) return st;
   for (int64_t m0 = 0; m0 < M; m0 += ls.nt) {
@@ -1090,7 +1152,6 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
     a.M = Mg;
     a.tok0 = (int)m0;
     if (i8_scale) {
-      a.y = y + m0 * A->N;
       st = launch_nt<true, EPI_I8>(ls, map, a, s);
     } else if (!argmax) {
       a.y = y + m0 * A->N;
@@ -1109,15 +1170,18 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
 
 }  // namespace
 
-// used by w12_cert.cu: y[M x V] = scale[v] * (x . codes^T) for an INT8 head whose code plane
-// (hi-plane layout) is codes; ws as for w12_gemm.
+// used by w12_cert.cu: the approximate logits scale[v] * (x . codes^T) of an INT8 head whose
+// code plane (hi-plane layout) is codes, fed to the certified argmax's threshold and
+// candidate superset (CertEpi); ws as for w12_gemm.
 int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float* scale, int64_t V, int64_t K,
-                 float* y, void* ws, size_t ws_bytes, cudaStream_t s, const char* fn) {
+                 const float* nx, const float* cb, uint32_t* thr_key, uint32_t* sup_count, uint2* sup,
+                 int64_t ldsup, void* ws, size_t ws_bytes, cudaStream_t s, const char* fn) {
   w12_matrix A{};
   A.N = V;
   A.K = K;
   A.hi = const_cast<uint8_t*>(codes);
-  return run_gemm(x, M, &A, y, nullptr, true, false, ws, ws_bytes, s, fn, scale);
+  const CertEpi cert{nx, cb, thr_key, sup_count, sup, ldsup};
+  return run_gemm(x, M, &A, nullptr, nullptr, true, false, ws, ws_bytes, s, fn, scale, &cert);
 }
 
 // used by w12_verify.cu
