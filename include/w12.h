@@ -157,7 +157,8 @@ W12_API int w12_export_canonical(const w12_matrix* A, uint8_t* hi_out, uint8_t* 
 
 /* Workspace bytes for w12_gemm / w12_gemm_q8 with these shapes on the current
  * device.  The workspace's first w12_gemm_counter_bytes(N) bytes (an error word
- * in the first 256 bytes, then one tile counter per row block) must be zero
+ * in the first 256 bytes, then one tile counter per row tile: four per 128-row
+ * block) must be zero
  * before the first call; every call that completes without a device error
  * leaves them zero again, and w12_workspace_status clears them after one. */
 W12_API size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K);

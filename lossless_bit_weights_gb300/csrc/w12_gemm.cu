@@ -274,14 +274,6 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target) {
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Rendezvous of a decode group's four warps (all 128 threads arrive) on an mbarrier, bounded.
-__device__ __forceinline__ bool epi_sync(uint32_t bar, uint32_t& phase, int lane) {
-  (void)lane;
-  mbar_arrive(bar);
-  const bool ok = warp_wait(bar, phase & 1u);
-  ++phase;
-  return ok;
-}
 
 // Output of 16 token columns [c0, c0+16) for this warp's 32 rows (row tile rt).
 template <int EPI>
@@ -629,7 +621,6 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     const int g = lane >> 2, t = lane & 3;
     // unit j decodes into A buffer j % AB; au counts the buffer's earlier uses (its phase)
     uint8_t* const abase = smem + P::kOffA + tl * (kTileRows * 128);
-    const uint32_t epi_bar = epi0 + 8 * gi;
     int ab = gi % AB;
     uint32_t au = (uint32_t)(gi / AB);
     const int KC = (int)a.KC, U0 = (int)u0;
@@ -640,7 +631,6 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     uint32_t ph = (uint32_t)((j / S) & 1);
     int cur_rb = -1;
     uint32_t base2[4];
-    uint32_t epi_phase = 0;
     for (; j < nunp; j += kTcGroups) {
       const int rb = P::kWide ? 2 * srb + pipe : srb;
       if (!I8 && rb != cur_rb) {  // this unit starts a new row block for the group: its rows' bases
@@ -770,23 +760,16 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           tc_fence_before();
           mbar_arrive(acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
-          // The group's barrier orders every thread's slot stores before one thread's
-          // acquire-release increment of the block's counter, which publishes them at GPU
-          // scope; the last arriver's increment acquires every other CTA's.
-          if (!epi_sync(epi_bar, epi_phase, lane)) {
-            bail = true;
-            break;
-          }
-          if (tl == 0 && lane == 0) misc[1 + gi] = atom_add_acq_rel(a.counters + rb, 1u);
-          if (!epi_sync(epi_bar, epi_phase, lane)) {
-            bail = true;
-            break;
-          }
-          const bool emit = (int64_t)misc[1 + gi] == ncov - 1;
-          if (!epi_sync(epi_bar, epi_phase, lane)) {
-            bail = true;
-            break;
-          }
+          // Each warp publishes its own row tile: the warp barrier orders its lanes' slot
+          // stores before lane 0's acquire-release increment of the tile's counter, which
+          // publishes them at GPU scope; the last arriver's increment acquires every other
+          // part's, and the second barrier orders the lanes' reads after it.
+          __syncwarp();
+          uint32_t arrived = 0u;
+          if (lane == 0) arrived = atom_add_acq_rel(a.counters + rb * kBlockTiles + tl, 1u);
+          arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+          __syncwarp();
+          const bool emit = (int64_t)arrived == ncov - 1;
           // At the pipeline's last unit every record stage and A buffer has been consumed
           // (the accumulator barrier follows every MMA, and each MMA follows its unit's
           // decode): each warp of the group then takes a quarter of that space and fetches
@@ -796,7 +779,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           constexpr int kQuarter = ((P::kOffBar - P::kOffA) / 4) & ~(kPiece - 1);
           const int per = kQuarter / (kPiece * (int)ncov);  // column chunks per batch
           if (emit && j == nunp - 1 && per >= 1) {
-            if (tl == 0 && lane == 0) a.counters[rb] = 0u;
+            if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
             const uint32_t sc = sbase + P::kOffA + tl * kQuarter;
             const uint32_t fb = smem_u32(misc + 4 + 2 * tl);
             if (lane == 0) {
@@ -847,7 +830,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
             }
             if (bail) break;
           } else if (emit) {
-            if (tl == 0 && lane == 0) a.counters[rb] = 0u;
+            if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
 #pragma unroll 1
             for (int c0 = 0; c0 < NT; c0 += 16) {
               float v[16];
@@ -998,7 +981,7 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   WsLayout L{};
   L.error = 0;
   L.counters = 256;
-  size_t off = 256 + align256((size_t)RB * 4);
+  size_t off = 256 + align256((size_t)RB * kBlockTiles * 4);
   L.slots = off;  // one slot of 128 channels x nt tokens per (partition part, row block) pair
   off = align256(off + (size_t)n_slots * (size_t)(kBlockTiles * kTileRows) * (size_t)ls.nt * 4);
   L.xpad = off;
@@ -1202,7 +1185,9 @@ using namespace w12;
 
 extern "C" {
 
-size_t w12_gemm_counter_bytes(int64_t N) { return N >= 1 ? 256 + align256((size_t)row_blocks(N) * 4) : 0; }
+size_t w12_gemm_counter_bytes(int64_t N) {
+  return N >= 1 ? 256 + align256((size_t)row_blocks(N) * kBlockTiles * 4) : 0;
+}
 
 size_t w12_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || N < 1 || K < 1 || K > kMaxK) return 0;

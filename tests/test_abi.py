@@ -108,4 +108,4 @@ def test_error_queries_and_noalloc_check_arguments_before_any_cuda_call():
     assert lib.w12_gemm_noalloc(p, 4, ctypes.byref(mis), p, None) == 1
     assert b"aligned" in lib.w12_last_error()
     assert lib.w12_gemm_noalloc(p, 0, ctypes.byref(A), p, None) == 2
-    assert lib.w12_gemm_counter_bytes(5120) == 256 + 256       # error word, then 40 counters
+    assert lib.w12_gemm_counter_bytes(5120) == 256 + 768       # error word, then 40 x 4 counters
