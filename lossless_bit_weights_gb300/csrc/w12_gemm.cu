@@ -199,18 +199,23 @@ struct TcPlan {
   static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
-  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[AB] a_empty[AB] epi[G] acc_full acc_empty mma_done
+  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[AB] a_empty[AB] acc_full1 acc_empty1 acc_full
+  // acc_empty mma_done (the first two: the second accumulator's)
   static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 2 * kABufs + kGroups + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kPipeBytes = (kBytes + 1023) / 1024 * 1024;
   static constexpr int kCtaBytes = kPipes == 1 ? kBytes : kXRegion + kPipes * kPipeBytes;
   static constexpr int kTmemCols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+  // accumulators per pipeline: with two, the MMAs of a row block's first unit do not wait
+  // for the drain of the row block before (segments alternate between them).  Measured
+  // faster for the 12-bit pass at 16 tokens; the 8-bit view and larger token tiles keep one.
+  static constexpr int kAccBufs = !Q8 && NT <= 32 ? 2 : 1;
   static_assert(kStages >= 3 && kStages > kGroups, "record ring too shallow");
   static_assert(kABufs >= kGroups, "an A buffer per decode group at least");
   static_assert(kCtaBytes <= 227 * 1024, "shared memory plan too large");
   static_assert(MODE != kModeOwn || NT <= 32, "launch mode does not fit the token tile");
-  static_assert(kPipes * kTmemCols <= 512, "tensor memory plan too large");
+  static_assert(kPipes * kAccBufs * kTmemCols <= 512, "tensor memory plan too large");
 };
 
 // 16 INT8 codes (sign<<7 | |q|, in the hi-plane byte order) -> 8 exact bf16 pairs.  A byte
@@ -405,7 +410,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       mbar_init(a_full0 + 8 * i, kBlockTiles * 32);
       mbar_init(a_empty0 + 8 * i, 1);
     }
-    for (int i = 0; i < kTcGroups; ++i) mbar_init(epi0 + 8 * i, kBlockTiles * 32);
+    mbar_init(epi0, 1);                        // second accumulator full
+    mbar_init(epi0 + 8, kBlockTiles * 32);     // second accumulator drained
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kBlockTiles * 32);
     mbar_init(mma_done, 1);
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   uint32_t* misc0 = reinterpret_cast<uint32_t*>(smem_cta + P::kXRegion + P::kOffMisc);
   if (warp == kTcMma && pipe == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc0)),
-                 "n"(P::kPipes * P::kTmemCols)
+                 "n"(P::kPipes * P::kAccBufs * P::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem0 = misc0[0];  // kept in a register: the teardown frees exactly this
-  const uint32_t tmem = tmem0 + (uint32_t)(pipe * P::kTmemCols);
+  const uint32_t tmem = tmem0 + (uint32_t)(pipe * P::kAccBufs * P::kTmemCols);
   bool bail = false, bad_index = false;
 
   if (!active) {
@@ -564,7 +570,10 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       uint32_t xph = 0, aph = 0;
       for (int j = 0; j < nunp; ++j) {
         const bool first = (j == 0) || (kc == 0);
-        if (first && j > 0 && !peer_wait(acc_empty, (uint32_t)((seg - 1) & 1))) {
+        const int abuf = P::kAccBufs == 2 ? (seg & 1) : 0;
+        // a segment's first MMAs wait for the drain of the accumulator's previous segment
+        if (first && seg >= P::kAccBufs &&
+            !peer_wait(abuf ? epi0 + 8 : acc_empty, (uint32_t)((seg / P::kAccBufs - 1) & 1))) {
           bail = true;
           break;
         }
@@ -576,11 +585,11 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
         const uint64_t ad = ad0 + (uint64_t)((ab * kABuf) >> 4), xd = xd0 + (uint64_t)((s * P::kX) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem, ad + 2 * ks, xd + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
+          umma_bf16(tmem + (uint32_t)(abuf * P::kTmemCols), ad + 2 * ks, xd + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
         umma_commit(a_empty0 + 8 * ab);
         umma_commit(x_empty0 + 8 * s);
         if (kc + 1 == KC || j + 1 == nunp) {
-          umma_commit(acc_full);
+          umma_commit(abuf ? epi0 : acc_full);
           ++seg;
         }
         if (++kc == KC) kc = 0;
@@ -722,14 +731,15 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           bail = true;
           break;
         }
-        if (!warp_wait(acc_full, (uint32_t)(seg & 1))) {
+        const int abuf = P::kAccBufs == 2 ? (seg & 1) : 0;
+        if (!warp_wait(abuf ? epi0 : acc_full, (uint32_t)((seg / P::kAccBufs) & 1))) {
           bail = true;
           break;
         }
         tc_fence_after();
         const int64_t rt = (int64_t)rb * kBlockTiles + tl;
         const bool whole = U0 <= srb * KC && kc == KC - 1;
-        const uint32_t trow = tmem + ((uint32_t)(tl * 32) << 16);
+        const uint32_t trow = tmem + (uint32_t)(abuf * P::kTmemCols) + ((uint32_t)(tl * 32) << 16);
         if (whole) {
 #pragma unroll 1
           for (int c0 = 0; c0 < NT; c0 += 16) {
@@ -738,7 +748,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
             emit_cols<EPI>(a, rt, lane, c0, v);
           }
           tc_fence_before();
-          mbar_arrive(acc_empty);
+          mbar_arrive(abuf ? epi0 + 8 : acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
         } else {
           const int64_t cf = cta_of_unit((int64_t)srb * KC, a.G, a.T);
@@ -758,7 +768,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
               __stcg(slot + (c0 / 4 + i) * 32 + lane, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
           }
           tc_fence_before();
-          mbar_arrive(acc_empty);
+          mbar_arrive(abuf ? epi0 + 8 : acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
           // Each warp publishes its own row tile: the warp barrier orders its lanes' slot
           // stores before lane 0's acquire-release increment of the tile's counter, which
@@ -878,7 +888,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   __syncthreads();
   tc_fence_after();
   if (warp == kTcMma && pipe == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem0), "n"(P::kPipes * P::kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem0),
+                 "n"(P::kPipes * P::kAccBufs * P::kTmemCols)
                  : "memory");
 }
 
