@@ -166,13 +166,18 @@ struct TcPlan {
   static constexpr int kParts = MODE == kModeOwn ? 2 : 1;     // places in the partition per CTA
   static constexpr int kGroups = 2;
   static constexpr int kDecoders = kGroups * kBlockTiles;
-  static constexpr int kRoles = kWide ? 2 : 3;                // producer, MMA issuer (, x warp)
-  static constexpr int kProducer = kDecoders, kMma = kDecoders + 1, kXWarp = kDecoders + 2;
+  // producer, MMA issuer (, publisher, x loader; the wide CTA's x loader is shared, after
+  // the pipelines).  A publisher measured faster with one or two own ranges per CTA; with
+  // row-block pairs the decode loop's register allocation moved and it lost.
+  static constexpr bool kHasPub = !kWide;
+  static constexpr int kRoles = kWide ? 2 : 4;
+  static constexpr int kProducer = kDecoders, kMma = kDecoders + 1, kPub = kDecoders + 2;
+  static constexpr int kXWarp = kWide ? kDecoders + 2 : kDecoders + 3;
   static constexpr int kThreads = (kDecoders + kRoles) * 32;  // one pipeline
   static constexpr int kCtaThreads = kPipes * kThreads + (kWide ? 32 : 0);
   static constexpr int kCtasPerSM = 1;
-  // Warps are spread over the SM's four sub-partitions (16K registers each); a 21- or
-  // 22-warp CTA puts six on one, so 80 registers a thread is the most that launches.
+  // Warps are spread over the SM's four sub-partitions (16K registers each); a 21- to
+  // 24-warp CTA puts six on one, so 80 registers a thread is the most that launches.
   static constexpr int kBoundThreads = kPipes == 1 ? kCtaThreads : kCtaThreads > 704 ? kCtaThreads : 704;
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
   // x stages: at 192 tokens with row-block pairs a third 24 KB stage (shared by both
@@ -199,9 +204,10 @@ struct TcPlan {
   static constexpr int kStagesRaw = (kBudget - kOffRec - 64 * 8 - 64) / kRec;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kOffBar = kOffRec + kStages * kRec;
-  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[AB] a_empty[AB] acc_full1 acc_empty1 acc_full
-  // acc_empty mma_done (the first two: the second accumulator's)
-  static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 2 * kABufs + kGroups + 3;
+  // rec_full[S] rec_empty[S] (x_full[SX] x_empty[SX]) a_full[AB] a_empty[AB] epi[2] acc_full
+  // acc_empty mma_done (pub); epi: the second accumulator's full and drained barriers; pub:
+  // a range's first row drained, for the publisher
+  static constexpr int kNumBars = 2 * kStages + (kWide ? 0 : 2 * kXStages) + 2 * kABufs + kGroups + 3 + (kHasPub ? 1 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kPipeBytes = (kBytes + 1023) / 1024 * 1024;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   constexpr bool I8 = EPI == EPI_I8;  // INT8 codes: no window bases, escapes or lo plane
   static_assert(!I8 || Q8, "INT8 codes use the 8-bit record plan");
   constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups, AB = P::kABufs;
-  constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcX = P::kXWarp;
+  constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcPub = P::kPub, kTcX = P::kXWarp;
   extern __shared__ __align__(1024) uint8_t smem_cta[];
   const int lane = threadIdx.x & 31, gwarp = threadIdx.x >> 5;
   // pipeline and the warp's role index inside it: the decode warps of pipeline p are
@@ -379,8 +385,8 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   const uint32_t x_full0 = P::kWide ? xbase + P::kOffXBar : bar0 + 16 * S, x_empty0 = x_full0 + 8 * SX;
   const uint32_t a_full0 = bar0 + 16 * S + (P::kWide ? 0 : 16 * SX), a_empty0 = a_full0 + 8 * AB;
   const uint32_t epi0 = a_empty0 + 8 * AB;
-  const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8;
-  // misc: [0] TMEM address, [1+g] stream-K flag of group g, [15] drains finished (four per segment)
+  const uint32_t acc_full = epi0 + 8 * kTcGroups, acc_empty = acc_full + 8, mma_done = acc_empty + 8, pub = mma_done + 8;
+  // misc: [0] TMEM address, [4..11] bulk fix-up barriers, [15] drains finished (four per segment)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
   const int64_t u0 = active ? b * a.T / a.G : 0, u1 = active ? (b + 1) * a.T / a.G : 0;
   const int nun = (int)(u1 - u0);
@@ -415,6 +421,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kBlockTiles * 32);
     mbar_init(mma_done, 1);
+    if (P::kHasPub) mbar_init(pub, kBlockTiles * 32);
     mbar_init_fence();
   }
   // one warp allocates the TMEM columns of every pipeline (address in pipeline 0's misc[0])
@@ -621,6 +628,54 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       }
     }
     __syncwarp();
+  } else if (P::kHasPub && warp == kTcPub) {
+    // ---------------------------------------------------------------- publisher
+    // A range that starts inside a row block and goes on past it drains that row early:
+    // its group signals here instead of publishing, and this warp publishes the row's four
+    // tiles and, when it is their last arrival, adds the parts' slots.
+    const int KC = (int)a.KC, U0 = (int)u0;
+    const int srb0 = U0 / KC;
+    if (nunp > 0 && (U0 % KC) != 0 && (U0 + nunp - 1) / KC > srb0) {
+      if (!warp_wait(pub, 0u)) {
+        bail = true;
+      } else {
+        const int rb = P::kWide ? 2 * srb0 + pipe : srb0;
+        const int64_t cf = cta_of_unit((int64_t)srb0 * KC, a.G, a.T);
+        const int64_t cl = cta_of_unit((int64_t)(srb0 + 1) * KC - 1, a.G, a.T);
+        const int64_t ncov = cl - cf + 1;
+        constexpr int kWarpSlot = NT * 32;
+        // lane t < 4 publishes row tile t: the barrier's acquire, then this release
+        uint32_t arrived = 0u;
+        if (lane < kBlockTiles) arrived = atom_add_acq_rel(a.counters + rb * kBlockTiles + lane, 1u);
+        const uint32_t last = __ballot_sync(0xFFFFFFFFu, lane < kBlockTiles && (int64_t)arrived == ncov - 1);
+        __syncwarp();  // the lanes' reads below follow the acquiring lane's increment
+#pragma unroll 1
+        for (int t = 0; t < kBlockTiles; ++t) {
+          if (!((last >> t) & 1u)) continue;
+          if (lane == 0) a.counters[rb * kBlockTiles + t] = 0u;
+          const int64_t rt = (int64_t)rb * kBlockTiles + t;
+#pragma unroll 1
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int64_t jj = 0; jj < ncov; ++jj) {
+              const int64_t slot = P::kWide ? 2 * (cf + jj + srb0) + pipe : cf + jj + srb0;
+              const float4* sj = reinterpret_cast<const float4*>(a.slots + (slot * kBlockTiles + t) * kWarpSlot);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 q4 = __ldcg(sj + (c0 / 4 + i) * 32 + lane);
+                v[4 * i] += q4.x;
+                v[4 * i + 1] += q4.y;
+                v[4 * i + 2] += q4.z;
+                v[4 * i + 3] += q4.w;
+              }
+            }
+            emit_cols<EPI>(a, rt, lane, c0, v);
+          }
+        }
+      }
+    }
   } else {
     // ---------------------------------------------------------------- decode warps
     // Group gi visits only its own units j = gi, gi+G, ...; row block, chunk,
@@ -770,95 +825,102 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           tc_fence_before();
           mbar_arrive(abuf ? epi0 + 8 : acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
-          // Each warp publishes its own row tile: the warp barrier orders its lanes' slot
-          // stores before lane 0's acquire-release increment of the tile's counter, which
-          // publishes them at GPU scope; the last arriver's increment acquires every other
-          // part's, and the second barrier orders the lanes' reads after it.
-          __syncwarp();
-          uint32_t arrived = 0u;
-          if (lane == 0) arrived = atom_add_acq_rel(a.counters + rb * kBlockTiles + tl, 1u);
-          arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
-          __syncwarp();
-          const bool emit = (int64_t)arrived == ncov - 1;
-          // At the pipeline's last unit every record stage and A buffer has been consumed
-          // (the accumulator barrier follows every MMA, and each MMA follows its unit's
-          // decode): each warp of the group then takes a quarter of that space and fetches
-          // the parts' slots with bulk copies, all in flight at once, where the fallback
-          // below waits for one L2 round trip per slot.  Both add the slots in part order.
-          constexpr int kPiece = 16 * 32 * 4;  // 16 token columns of one warp's slot
-          constexpr int kQuarter = ((P::kOffBar - P::kOffA) / 4) & ~(kPiece - 1);
-          const int per = kQuarter / (kPiece * (int)ncov);  // column chunks per batch
-          if (emit && j == nunp - 1 && per >= 1) {
-            if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
-            const uint32_t sc = sbase + P::kOffA + tl * kQuarter;
-            const uint32_t fb = smem_u32(misc + 4 + 2 * tl);
-            if (lane == 0) {
-              mbar_init(fb, 1);
-              mbar_init_fence();
-              fence_proxy_async_smem();    // earlier generic accesses of the space -> the copies
-              fence_proxy_async_global();  // the other parts' slots, acquired above -> the copies
-            }
+          if (P::kHasPub && j != nunp - 1) {
+            // A partial row that ends before the range does is the range's first: the
+            // publisher warp publishes it, and this group goes on decoding.  The barrier's
+            // release orders each thread's slot stores before the publisher's increment.
+            mbar_arrive(pub);
+          } else {
+            // Each warp publishes its own row tile: the warp barrier orders its lanes' slot
+            // stores before lane 0's acquire-release increment of the tile's counter, which
+            // publishes them at GPU scope; the last arriver's increment acquires every other
+            // part's, and the second barrier orders the lanes' reads after it.
             __syncwarp();
-            const uint64_t pol_s = policy_evict_first();
-            uint32_t fph = 0;
-#pragma unroll 1
-            for (int c = 0; c < NT / 16 && !bail; c += per) {
-              const int nb = min(per, NT / 16 - c);
+            uint32_t arrived = 0u;
+            if (lane == 0) arrived = atom_add_acq_rel(a.counters + rb * kBlockTiles + tl, 1u);
+            arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+            __syncwarp();
+            const bool emit = (int64_t)arrived == ncov - 1;
+            // At the pipeline's last unit every record stage and A buffer has been consumed
+            // (the accumulator barrier follows every MMA, and each MMA follows its unit's
+            // decode): each warp of the group then takes a quarter of that space and fetches
+            // the parts' slots with bulk copies, all in flight at once, where the fallback
+            // below waits for one L2 round trip per slot.  Both add the slots in part order.
+            constexpr int kPiece = 16 * 32 * 4;  // 16 token columns of one warp's slot
+            constexpr int kQuarter = ((P::kOffBar - P::kOffA) / 4) & ~(kPiece - 1);
+            const int per = kQuarter / (kPiece * (int)ncov);  // column chunks per batch
+            if (emit && j == nunp - 1 && per >= 1) {
+              if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
+              const uint32_t sc = sbase + P::kOffA + tl * kQuarter;
+              const uint32_t fb = smem_u32(misc + 4 + 2 * tl);
               if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)(nb * ncov * kPiece));
-                for (int cc = 0; cc < nb; ++cc)
-                  for (int64_t jj = 0; jj < ncov; ++jj)
-                    bulk_g2s(sc + (uint32_t)((cc * ncov + jj) * kPiece),
-                             a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot + (c + cc) * 16 * 32, kPiece,
-                             fb, pol_s);
+                mbar_init(fb, 1);
+                mbar_init_fence();
+                fence_proxy_async_smem();    // earlier generic accesses of the space -> the copies
+                fence_proxy_async_global();  // the other parts' slots, acquired above -> the copies
               }
-              if (!warp_wait(fb, fph)) {
-                if (lane == 0) mbar_wait_bounded(fb, fph);  // copies in flight land before the CTA leaves
-                bail = true;
-                break;
-              }
-              fph ^= 1u;
+              __syncwarp();
+              const uint64_t pol_s = policy_evict_first();
+              uint32_t fph = 0;
 #pragma unroll 1
-              for (int cc = 0; cc < nb; ++cc) {
+              for (int c = 0; c < NT / 16 && !bail; c += per) {
+                const int nb = min(per, NT / 16 - c);
+                if (lane == 0) {
+                  mbar_arrive_expect_tx(fb, (uint32_t)(nb * ncov * kPiece));
+                  for (int cc = 0; cc < nb; ++cc)
+                    for (int64_t jj = 0; jj < ncov; ++jj)
+                      bulk_g2s(sc + (uint32_t)((cc * ncov + jj) * kPiece),
+                               a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot + (c + cc) * 16 * 32, kPiece,
+                               fb, pol_s);
+                }
+                if (!warp_wait(fb, fph)) {
+                  if (lane == 0) mbar_wait_bounded(fb, fph);  // copies in flight land before the CTA leaves
+                  bail = true;
+                  break;
+                }
+                fph ^= 1u;
+#pragma unroll 1
+                for (int cc = 0; cc < nb; ++cc) {
+                  float v[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                  for (int64_t jj = 0; jj < ncov; ++jj) {
+                    const uint32_t pc = sc + (uint32_t)((cc * ncov + jj) * kPiece) + (uint32_t)lane * 16u;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      const uint4 q4 = lds128(pc + (uint32_t)i * 512u);
+                      v[4 * i] += __uint_as_float(q4.x);
+                      v[4 * i + 1] += __uint_as_float(q4.y);
+                      v[4 * i + 2] += __uint_as_float(q4.z);
+                      v[4 * i + 3] += __uint_as_float(q4.w);
+                    }
+                  }
+                  emit_cols<EPI>(a, rt, lane, (c + cc) * 16, v);
+                }
+                __syncwarp();  // every lane has read the batch before the next one lands
+              }
+              if (bail) break;
+            } else if (emit) {
+              if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
+#pragma unroll 1
+              for (int c0 = 0; c0 < NT; c0 += 16) {
                 float v[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 for (int64_t jj = 0; jj < ncov; ++jj) {
-                  const uint32_t pc = sc + (uint32_t)((cc * ncov + jj) * kPiece) + (uint32_t)lane * 16u;
+                  const float4* sj =
+                      reinterpret_cast<const float4*>(a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot);
 #pragma unroll
                   for (int i = 0; i < 4; ++i) {
-                    const uint4 q4 = lds128(pc + (uint32_t)i * 512u);
-                    v[4 * i] += __uint_as_float(q4.x);
-                    v[4 * i + 1] += __uint_as_float(q4.y);
-                    v[4 * i + 2] += __uint_as_float(q4.z);
-                    v[4 * i + 3] += __uint_as_float(q4.w);
+                    const float4 q4 = __ldcg(sj + (c0 / 4 + i) * 32 + lane);
+                    v[4 * i] += q4.x;
+                    v[4 * i + 1] += q4.y;
+                    v[4 * i + 2] += q4.z;
+                    v[4 * i + 3] += q4.w;
                   }
                 }
-                emit_cols<EPI>(a, rt, lane, (c + cc) * 16, v);
+                emit_cols<EPI>(a, rt, lane, c0, v);
               }
-              __syncwarp();  // every lane has read the batch before the next one lands
-            }
-            if (bail) break;
-          } else if (emit) {
-            if (lane == 0) a.counters[rb * kBlockTiles + tl] = 0u;
-#pragma unroll 1
-            for (int c0 = 0; c0 < NT; c0 += 16) {
-              float v[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              for (int64_t jj = 0; jj < ncov; ++jj) {
-                const float4* sj =
-                    reinterpret_cast<const float4*>(a.slots + (slot_of(cf + jj) * kBlockTiles + tl) * kWarpSlot);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float4 q4 = __ldcg(sj + (c0 / 4 + i) * 32 + lane);
-                  v[4 * i] += q4.x;
-                  v[4 * i + 1] += q4.y;
-                  v[4 * i + 2] += q4.z;
-                  v[4 * i + 3] += q4.w;
-                }
-              }
-              emit_cols<EPI>(a, rt, lane, c0, v);
             }
           }
         }
