@@ -53,6 +53,25 @@ def test_ragged_shapes(w12, M, N, K, q8):
     check(w12, W, x, q8)
 
 
+@pytest.mark.parametrize("M,N,K,q8", [(16, 256, 17408, False), (16, 256, 17408, True), (32, 200, 12000, False),
+                                      (192, 256, 17408, False)])
+def test_many_parts_per_row_block(w12, M, N, K, q8):
+    """Long rows over few row blocks: each row block is split over dozens of parts, so the
+    last arrival adds more slots than a warp's share of shared memory holds (the register
+    path) and most ranges start inside a row block (published early by their pipeline's
+    publisher warp).  Repeats stay bit-identical."""
+    W = synth.weights(3, M, N * 5 + K, N, K)
+    x = synth.activations(2, M, K, M, K)
+    ws = w12.Workspace()
+    check(w12, W, x, q8, ws=ws)
+    A = w12.encode(to_dev16(W))
+    fn = w12.w12_gemm_q8 if q8 else w12.w12_gemm
+    y0 = fn(to_dev16(x), A, ws=ws)
+    y1 = fn(to_dev16(x), A, ws=ws)
+    assert torch.equal(y0, y1)
+    assert ws.status() == 0
+
+
 def test_exact_on_small_integers(w12):
     """Integer-valued weights and activations with small magnitudes: every
     partial sum is exact in fp32, so the GPU result equals the integer GEMM."""
