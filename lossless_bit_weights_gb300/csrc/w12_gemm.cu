@@ -15,15 +15,20 @@
 //    K read as zero);
 //  - two groups of four decode warps take alternate units; each warp decodes
 //    its 32x64 tile in registers to bf16 (sign, base+offset, mantissa), stores
-//    it to the group's swizzled A buffer and writes the tile's escapes over
-//    their slots;
+//    it to a swizzled A buffer (the buffers rotate over the units) and writes
+//    the tile's escapes over their slots;
 //  - one thread issues tcgen05.mma (M = 128 channels, N = 16..256 tokens,
 //    swap-AB: weights on the M side) with the fp32 accumulator in tensor
-//    memory; at the end of a row block the group that decoded its last unit
+//    memory (two, alternating by row block, for the 12-bit pass up to 32
+//    tokens); at the end of a row block the group that decoded its last unit
 //    reads the accumulator back;
-//  - a CTA that owns part of a row block writes partial sums to a fixed slot;
-//    the last CTA of that block to arrive (atomic counter, no waiting) adds
-//    the slots in slot order, so results are bit-identical from call to call;
+//  - a part of the partition that covers only some of a row block writes
+//    partial sums to a fixed slot and publishes each row tile with an atomic
+//    counter; the last part to arrive (no waiting) adds the slots in part
+//    order, so results are bit-identical from call to call.  At a range's end
+//    it fetches them by bulk copy into the consumed ring; a range's first row,
+//    drained early, is published by a publisher warp while the decode goes on
+//    (with one or two own ranges per CTA);
 //  - launches use programmatic dependent launch: a GEMM starts streaming its
 //    weights while the previous kernel on the stream drains, and waits for
 //    that kernel only before it reads x.
