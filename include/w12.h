@@ -389,6 +389,12 @@ W12_API int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head
  *     o_t = S_t q_t.
  * dk, dv <= 256 with (dk * (dv + 1) + dk + dv) * 4 <= 200 KB (W12_ERR_SHAPE
  * otherwise).
+ * The three calls use programmatic dependent launch: gdn_path_verify and
+ * gdn_wy_verify let the next kernel on the stream start early and read S0
+ * before they wait for the previous kernel (their other inputs after it), so
+ * S0 must not be written by the kernel just before them unless that kernel
+ * never signals early (gdn_commit does not); gdn_commit waits for the previous
+ * kernel before it reads anything.
  */
 
 /* s1 = bf16_rne(x), s2 = bf16_rne(x - s1), s3 = bf16_rne(x - s1 - s2) (float

@@ -338,6 +338,12 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_path_verify_reg(
   __shared__ int32_t path[kGdnMaxNodes];
   __shared__ int32_t plen;
   const int64_t i = blockIdx.x, h = blockIdx.y, r0 = (int64_t)blockIdx.z * kRegRows;
+  // the next kernel on the stream may start now (programmatic dependent launch); the state
+  // is read before this one waits for the previous kernel, the node inputs after
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  RegState<DK> S;
+  reg_load<DK>(S, S0 + (h * dv + r0) * DK, dv - r0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     int32_t L = 0;
     bool ok = parent[0] == -1;
@@ -356,8 +362,6 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_path_verify_reg(
     }
     plen = L;
   }
-  RegState<DK> S;
-  reg_load<DK>(S, S0 + (h * dv + r0) * DK, dv - r0);
   __syncthreads();
   const int32_t L = plen;
   if (L < 0) return;
@@ -386,6 +390,9 @@ __global__ void __launch_bounds__(kRegThreads) k_gdn_commit_reg(
   constexpr int Q = RegState<DK>::Q;
   __shared__ __align__(16) float kv[4 * (Q + 4) + kRegRows];
   const int64_t h = blockIdx.x, r0 = (int64_t)blockIdx.y * kRegRows;
+  // launched early behind a kernel that signals early, it waits for that kernel before it
+  // reads anything; it never signals early itself, since it writes the state
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t L = *path_len;
   if (L <= 0) return;
   if (L >= n) {
@@ -491,7 +498,10 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P::kTmem);
   int32_t* flag = reinterpret_cast<int32_t*>(sm + P::kFlag);
 
-  // ---- inputs: the head's state rows by one bulk copy, node scalars, node vectors
+  // ---- inputs: the head's state rows by one bulk copy, node scalars, node vectors.  The
+  // next kernel on the stream may start now (programmatic dependent launch); this one reads
+  // the state before it waits for the previous kernel, everything else after.
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     *flag = 0;
     mbar_init(bar_stage, 1);
@@ -507,6 +517,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy_verify_tc(
     for (uint32_t off = 0; off < bytes; off += 16384u)
       bulk_g2s(sbase + P::kStage + off, src + off, bytes - off < 16384u ? bytes - off : 16384u, bar_stage, pol);
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the node inputs may be the previous kernel's
   // Warps 0-3 stage v of their state rows for every node; warps 4-5 read the tree and build
   // each node's path mask and gamma; warps 6-15 zero the rows past dv and fill the node
   // tiles.  The state rows land meanwhile.
@@ -769,6 +780,24 @@ int set_gdn_smem(const void* kernel, size_t bytes) {
   return W12_OK;
 }
 
+// Launch configuration with programmatic dependent launch: the kernel may start while the
+// previous kernel on the stream drains (if that kernel signals early) and waits for it with
+// griddepcontrol.wait before reading that kernel's outputs.
+cudaLaunchConfig_t pdl_config(dim3 grid, int threads, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.stream = (cudaStream_t)stream;
+  return cfg;
+}
+
+void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
 }  // namespace
 }  // namespace w12
 
@@ -799,14 +828,16 @@ int gdn_path_verify(const float* S0, const uint16_t* q, const uint16_t* k, const
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   const bool aligned = (((uintptr_t)S0) & 15u) == 0;
   if (aligned && (dk == 128 || dk == 64)) {  // state in registers, 32 rows a block
-    const dim3 grid((unsigned)n, (unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
-    const int threads = kRegThreads;
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)n, (unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows)),
+                                         kRegThreads, stream);
+    cudaLaunchAttribute attr[1];
+    pdl_attr(cfg, attr);
     if (dk == 128)
-      k_gdn_path_verify_reg<128><<<grid, threads, 0, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
-                                                                             dv, O, status);
+      W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_path_verify_reg<128>, S0, q, k, v, alpha, beta, parent, n, H, dv, O,
+                                      status));
     else
-      k_gdn_path_verify_reg<64><<<grid, threads, 0, (cudaStream_t)stream>>>(S0, q, k, v, alpha, beta, parent, n, H,
-                                                                            dv, O, status);
+      W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_path_verify_reg<64>, S0, q, k, v, alpha, beta, parent, n, H, dv, O,
+                                      status));
     W12_LAUNCH_CHECK(fn);
     return W12_OK;
   }
@@ -831,15 +862,19 @@ int gdn_wy_verify(const float* S0, const uint16_t* q, const uint16_t* k, const u
   if (!S0 || !q || !k || !v || !alpha || !beta || !parent || !O || !status)
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if ((((uintptr_t)S0) & 15u) != 0) return fail(W12_ERR_INVALID_ARG, "%s: S0 must be 16-byte aligned", fn);
-  const dim3 grid((unsigned)H, (unsigned)((dv + kWyRows - 1) / kWyRows));
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)H, (unsigned)((dv + kWyRows - 1) / kWyRows)), kWyThreads, stream);
+  cudaLaunchAttribute attr[1];
+  pdl_attr(cfg, attr);
   if (dk == 128) {
     if ((st = set_gdn_smem((const void*)k_gdn_wy_verify_tc<128>, wy_tc_smem<128>()))) return st;
-    k_gdn_wy_verify_tc<128><<<grid, kWyThreads, wy_tc_smem<128>(), (cudaStream_t)stream>>>(
-        S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O, status);
+    cfg.dynamicSmemBytes = wy_tc_smem<128>();
+    W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_wy_verify_tc<128>, S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O,
+                                    status));
   } else {
     if ((st = set_gdn_smem((const void*)k_gdn_wy_verify_tc<64>, wy_tc_smem<64>()))) return st;
-    k_gdn_wy_verify_tc<64><<<grid, kWyThreads, wy_tc_smem<64>(), (cudaStream_t)stream>>>(
-        S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O, status);
+    cfg.dynamicSmemBytes = wy_tc_smem<64>();
+    W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_wy_verify_tc<64>, S0, q, k, v, alpha, beta, parent, (int)n, H, dv, O,
+                                    status));
   }
   W12_LAUNCH_CHECK(fn);
   return W12_OK;
@@ -855,13 +890,16 @@ int gdn_commit(float* S, const uint16_t* k, const uint16_t* v, const float* alph
   if (!S || !k || !v || !alpha || !beta || !path_len || !path_nodes || !status)
     return fail(W12_ERR_INVALID_ARG, "%s: null pointer", fn);
   if ((((uintptr_t)S) & 15u) == 0 && (dk == 128 || dk == 64)) {  // state in registers, 32 rows a block
-    const dim3 grid((unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows));
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)H, (unsigned)((dv + kRegRows - 1) / kRegRows)), kRegThreads,
+                                         stream);
+    cudaLaunchAttribute attr[1];
+    pdl_attr(cfg, attr);
     if (dk == 128)
-      k_gdn_commit_reg<128><<<grid, kRegThreads, 0, (cudaStream_t)stream>>>(S, k, v, alpha, beta, path_len, path_nodes,
-                                                                           n, H, dv, status);
+      W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_commit_reg<128>, S, k, v, alpha, beta, path_len, path_nodes, n, H, dv,
+                                      status));
     else
-      k_gdn_commit_reg<64><<<grid, kRegThreads, 0, (cudaStream_t)stream>>>(S, k, v, alpha, beta, path_len, path_nodes,
-                                                                          n, H, dv, status);
+      W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gdn_commit_reg<64>, S, k, v, alpha, beta, path_len, path_nodes, n, H, dv,
+                                      status));
     W12_LAUNCH_CHECK(fn);
     return W12_OK;
   }
