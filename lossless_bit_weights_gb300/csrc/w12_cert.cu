@@ -28,7 +28,8 @@ int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float
 
 namespace {
 
-constexpr int kExactBlocks = 256;  // blocks per row of the exact recompute
+constexpr int kFilterBlocks = 16;  // blocks per row of the candidate filter
+constexpr int kExactPerSM = 6;     // blocks per SM of the exact recompute
 constexpr int kExactWarps = 10;    // 10 x 8 chunks: K = 5120 in one round
 
 inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(256) k_i8_encode(const uint16_t* __restrict__ 
 // the row's threshold key and counters for the GEMM's epilogue and the exact recompute.
 __global__ void __launch_bounds__(256) k_cert_prep(const uint16_t* __restrict__ x, int64_t K, float* __restrict__ nx,
                                                    uint32_t* __restrict__ thr_key, int32_t* __restrict__ count,
-                                                   uint32_t* __restrict__ sup_count) {
+                                                   uint32_t* __restrict__ sup_count, uint32_t* __restrict__ n_list) {
   // the GEMM that follows may start streaming its weights; it reads nothing of ours
   // before its griddepcontrol.wait
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(256) k_cert_prep(const uint16_t* __restrict__ 
     thr_key[blockIdx.x] = 0u;
     count[blockIdx.x] = 0;
     sup_count[blockIdx.x] = 0u;
+    if (blockIdx.x == 0) *n_list = 0u;
   }
 }
 
@@ -164,127 +166,141 @@ __device__ __forceinline__ bool beats(double a, int32_t ia, double b, int32_t ib
   return a > b || (a == b && ia < ib);
 }
 
-// Exact logits of the candidates from the W12 head.  Block b of row m takes the superset
-// entries b, b + gridDim.x, ... (one per thread in each round), keeps those whose upper
-// bound reaches the row's final threshold (the candidates) in a shared list, and computes
-// each candidate with the whole block: lane 4*c8 + t of warp w decodes the 16 columns
-// 16t.. of chunks w*8 + c8 + 80i (the same decode as the GEMM) and patches the channel's
-// escapes in them.  A product of two bf16 values is exact in float; the sum is a float
-// pair (TwoSum), whose error is near 2^-48 of sum|x*w|, far inside the argmax's tie
-// tolerance and on the full-rate float pipe (float64 runs at a small fraction of it on
-// this GPU).  count[m] (zero beforehand) receives the number of candidates.
-__global__ void __launch_bounds__(kExactWarps * 32)
-    k_cert_exact(const uint16_t* __restrict__ x, int64_t K, int64_t KC, const uint8_t* __restrict__ hi,
-                 const uint8_t* __restrict__ lo, const uint8_t* __restrict__ base, const uint32_t* __restrict__ tile_ptr,
-                 const uint32_t* __restrict__ esc, const uint32_t* __restrict__ thr_key,
-                 const uint32_t* __restrict__ sup_count, const uint2* __restrict__ sup, int64_t ldsup,
-                 int32_t* __restrict__ count, DecodeMul mul, Best* __restrict__ part) {
-  // the final merge may launch now; everything here waits for the INT8 GEMM to complete
+// Candidates: the superset entries of row m whose upper bound reaches the row's final
+// threshold, appended to one list over all rows (entry: row, channel; the order varies
+// from call to call, the set does not).  count[m] and *n_list are zero beforehand.
+__global__ void __launch_bounds__(256) k_cert_filter(const uint32_t* __restrict__ thr_key,
+                                                     const uint32_t* __restrict__ sup_count,
+                                                     const uint2* __restrict__ sup, int64_t ldsup,
+                                                     int32_t* __restrict__ count, uint2* __restrict__ list,
+                                                     uint32_t* __restrict__ n_list) {
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float shh[kExactWarps], shl[kExactWarps];
-  __shared__ int32_t sh_cand[kExactWarps * 32];
-  __shared__ int sh_n;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the INT8 GEMM has completed
   const int64_t m = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c8 = lane >> 2, t = lane & 3;
+  const int lane = threadIdx.x & 31;
   const uint32_t n_sup = min(sup_count[m], (uint32_t)ldsup);
   const float thr = fkey_inv(thr_key[m]);
-  const uint16_t* xr = x + m * K;
-  Best best{0.0, -1};
-  int mine = 0;
-  for (uint32_t r0 = blockIdx.x; r0 < n_sup; r0 += gridDim.x * blockDim.x) {
-    if (threadIdx.x == 0) sh_n = 0;
-    __syncthreads();
-    const uint32_t e = r0 + threadIdx.x * gridDim.x;
+  for (uint32_t e0 = blockIdx.x * blockDim.x; e0 < n_sup; e0 += gridDim.x * blockDim.x) {
+    const uint32_t e = e0 + threadIdx.x;
+    bool keep = false;
+    uint32_t v = 0u;
     if (e < n_sup) {
       const uint2 ent = sup[m * ldsup + e];
-      if (fkey_inv(ent.y) >= thr) sh_cand[atomicAdd(&sh_n, 1)] = (int32_t)ent.x;
+      keep = fkey_inv(ent.y) >= thr;
+      v = ent.x;
     }
-    __syncthreads();
-    const int nc = sh_n;
-    mine += nc;
-    for (int i = 0; i < nc; ++i) {
-      const int64_t v = sh_cand[i];
-      const int64_t rt = v / kTileRows;
-      const int r = (int)(v % kTileRows), q = r >> 3, g = r & 7;
-      const uint32_t bb = base[v];
-      const uint32_t base2 = (bb << 7) | (bb << 23);
-      float ah = 0.f, al = 0.f;
-      for (int64_t kc = warp * 8 + c8; kc < KC; kc += kExactWarps * 8) {
-        const int64_t tile = tile_index(rt, kc, KC);
-        const uint4 hq = *reinterpret_cast<const uint4*>(hi + tile * kHiTileBytes + q * 512 + (4 * g + t) * 16);
-        const uint2 lq = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
-        const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
-        uint32_t pr[8];
-        decode16<false>(hq, lq, base2, mul, pr);
-        uint16_t w[16];
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          w[2 * p] = (uint16_t)(pr[p] & 0xFFFFu);
-          w[2 * p + 1] = (uint16_t)(pr[p] >> 16);
-        }
-        // the tile's escapes, four independent loads at a time
-        for (uint32_t e = e0; e < e1; e += 4) {
-          uint32_t ent[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) ent[u] = e + u < e1 ? esc[e + u] : 0xFFFFFFFFu;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = esc_col(ent[u]);
-            if (ent[u] != 0xFFFFFFFFu && esc_row(ent[u]) == r && (c >> 4) == t) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent[u]);
-            }
-          }
-        }
-        const int64_t k0 = kc * kTileK + 16 * t;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (k0 + j < K) acc2(ah, al, __fmul_rn(bf16f(xr[k0 + j]), bf16f(w[j])));
-      }
-      for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xFFFFFFFFu, ah, o), ol = __shfl_xor_sync(0xFFFFFFFFu, al, o);
-        acc2(ah, al, oh);
-        al = __fadd_rn(al, ol);
-      }
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+    if (bal) {
+      uint32_t p0 = 0u;
       if (lane == 0) {
-        shh[warp] = ah;
-        shl[warp] = al;
+        p0 = atomicAdd(n_list, (uint32_t)__popc(bal));
+        atomicAdd(count + m, __popc(bal));
       }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float h = shh[0], l = shl[0];
-        for (int w2 = 1; w2 < kExactWarps; ++w2) {
-          acc2(h, l, shh[w2]);
-          l = __fadd_rn(l, shl[w2]);
-        }
-        const double acc = (double)h + (double)l;
-        if (beats(acc, (int32_t)v, best.val, best.idx)) best = Best{acc, (int32_t)v};
-      }
-      __syncthreads();
+      p0 = __shfl_sync(0xFFFFFFFFu, p0, 0);
+      if (keep) list[p0 + (uint32_t)__popc(bal & ((1u << lane) - 1u))] = make_uint2((uint32_t)m, v);
     }
-    __syncthreads();  // every thread has read the round's count before the next round resets it
-  }
-  if (threadIdx.x == 0) {
-    part[m * gridDim.x + blockIdx.x] = best;
-    if (mine) atomicAdd(count + m, mine);
   }
 }
 
-// One block of 256 per row: thread i merges partials i and i + 256, then the warps and
-// the block merge in a fixed order.
-__global__ void __launch_bounds__(256) k_cert_final(const Best* __restrict__ part, const int32_t* __restrict__ count,
-                                                    int32_t* __restrict__ tok, int32_t* __restrict__ ncand) {
+// Exact logits of the listed candidates from the W12 head, val[i] for list entry i.  The
+// blocks take the entries i = b, b + gridDim.x, ... (a grid of a few blocks per SM keeps
+// every SM busy whatever the rows' candidate counts); the whole block computes one
+// candidate: lane 4*c8 + t of warp w decodes the 16 columns 16t.. of chunks w*8 + c8 + 80i
+// (the same decode as the GEMM) and patches the channel's escapes in them.  A product of
+// two bf16 values is exact in float; the sum is a float pair (TwoSum), whose error is near
+// 2^-48 of sum|x*w|, far inside the argmax's tie tolerance and on the full-rate float pipe
+// (float64 runs at a small fraction of it on this GPU).
+__global__ void __launch_bounds__(kExactWarps * 32)
+    k_cert_exact(const uint16_t* __restrict__ x, int64_t K, int64_t KC, const uint8_t* __restrict__ hi,
+                 const uint8_t* __restrict__ lo, const uint8_t* __restrict__ base, const uint32_t* __restrict__ tile_ptr,
+                 const uint32_t* __restrict__ esc, const uint2* __restrict__ list, const uint32_t* __restrict__ n_list,
+                 uint32_t cap, DecodeMul mul, double* __restrict__ val) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the candidate list is complete
+  __shared__ float shh[kExactWarps], shl[kExactWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c8 = lane >> 2, t = lane & 3;
+  const uint32_t n = min(*n_list, cap);
+  for (uint32_t i = blockIdx.x; i < n; i += gridDim.x) {
+    const uint2 ent = list[i];
+    const int64_t m = ent.x, v = ent.y;
+    const uint16_t* xr = x + m * K;
+    const int64_t rt = v / kTileRows;
+    const int r = (int)(v % kTileRows), q = r >> 3, g = r & 7;
+    const uint32_t bb = base[v];
+    const uint32_t base2 = (bb << 7) | (bb << 23);
+    float ah = 0.f, al = 0.f;
+    for (int64_t kc = warp * 8 + c8; kc < KC; kc += kExactWarps * 8) {
+      const int64_t tile = tile_index(rt, kc, KC);
+      const uint4 hq = *reinterpret_cast<const uint4*>(hi + tile * kHiTileBytes + q * 512 + (4 * g + t) * 16);
+      const uint2 lq = *reinterpret_cast<const uint2*>(lo + tile * kLoTileBytes + q * 256 + (4 * g + t) * 8);
+      const uint32_t e0 = tile_ptr[tile], e1 = tile_ptr[tile + 1];
+      uint32_t pr[8];
+      decode16<false>(hq, lq, base2, mul, pr);
+      uint16_t w[16];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        w[2 * p] = (uint16_t)(pr[p] & 0xFFFFu);
+        w[2 * p + 1] = (uint16_t)(pr[p] >> 16);
+      }
+      // the tile's escapes, four independent loads at a time
+      for (uint32_t e = e0; e < e1; e += 4) {
+        uint32_t ent4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ent4[u] = e + u < e1 ? esc[e + u] : 0xFFFFFFFFu;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = esc_col(ent4[u]);
+          if (ent4[u] != 0xFFFFFFFFu && esc_row(ent4[u]) == r && (c >> 4) == t) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j == (c & 15)) w[j] = (uint16_t)esc_raw(ent4[u]);
+          }
+        }
+      }
+      const int64_t k0 = kc * kTileK + 16 * t;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (k0 + j < K) acc2(ah, al, __fmul_rn(bf16f(xr[k0 + j]), bf16f(w[j])));
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xFFFFFFFFu, ah, o), ol = __shfl_xor_sync(0xFFFFFFFFu, al, o);
+      acc2(ah, al, oh);
+      al = __fadd_rn(al, ol);
+    }
+    if (lane == 0) {
+      shh[warp] = ah;
+      shl[warp] = al;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float h = shh[0], l = shl[0];
+      for (int w2 = 1; w2 < kExactWarps; ++w2) {
+        acc2(h, l, shh[w2]);
+        l = __fadd_rn(l, shl[w2]);
+      }
+      val[i] = (double)h + (double)l;
+    }
+    __syncthreads();
+  }
+}
+
+// One block of 256 per row: its threads scan the candidate list for the row's entries and
+// keep the largest exact logit (lowest channel on ties), then the warps and the block
+// merge; the result does not depend on the list's order.
+__global__ void __launch_bounds__(256) k_cert_final(const uint2* __restrict__ list, const double* __restrict__ val,
+                                                    const uint32_t* __restrict__ n_list, uint32_t cap,
+                                                    const int32_t* __restrict__ count, int32_t* __restrict__ tok,
+                                                    int32_t* __restrict__ ncand) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the exact recompute has completed
   __shared__ Best sh[8];
-  const int64_t m = blockIdx.x;
+  const uint32_t m = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t n = min(*n_list, cap);
   Best b{0.0, -1};
-  for (int i = threadIdx.x; i < kExactBlocks; i += 256) {
-    const Best c = part[m * kExactBlocks + i];
-    if (beats(c.val, c.idx, b.val, b.idx)) b = c;
+  for (uint32_t i = threadIdx.x; i < n; i += 256) {
+    const uint2 ent = list[i];
+    if (ent.x == m && beats(val[i], (int32_t)ent.y, b.val, b.idx)) b = Best{val[i], (int32_t)ent.y};
   }
   for (int o = 16; o > 0; o >>= 1) {
     const double ov = __shfl_xor_sync(0xFFFFFFFFu, b.val, o);
@@ -302,10 +318,11 @@ __global__ void __launch_bounds__(256) k_cert_final(const Best* __restrict__ par
 }
 
 struct CertWs {
-  size_t gemm, nx, thr, count, sup_count, sup, part, total;
+  size_t gemm, nx, thr, count, sup_count, n_list, sup, list, val, total;
 };
 
-// The candidate superset of a row holds at most one entry per channel: M x V entries.
+// A row's candidate superset, and the candidate list over all rows, hold at most one entry
+// per channel and row: M x V entries each.
 CertWs cert_ws(int64_t M, int64_t V, int64_t K) {
   CertWs L{};
   L.gemm = 0;
@@ -318,10 +335,14 @@ CertWs cert_ws(int64_t M, int64_t V, int64_t K) {
   off = al256(off + (size_t)M * 4);
   L.sup_count = off;
   off = al256(off + (size_t)M * 4);
+  L.n_list = off;
+  off = al256(off + 4);
   L.sup = off;
   off = al256(off + (size_t)M * (size_t)V * 8);
-  L.part = off;
-  off = al256(off + (size_t)M * kExactBlocks * sizeof(Best));
+  L.list = off;
+  off = al256(off + (size_t)M * (size_t)V * 8);
+  L.val = off;
+  off = al256(off + (size_t)M * (size_t)V * 8);
   L.total = off;
   return L;
 }
@@ -384,34 +405,49 @@ int w12_cert_head_argmax(const uint16_t* x, int64_t M, const w12_i8_head* H, con
   uint32_t* thr = reinterpret_cast<uint32_t*>(w + L.thr);
   int32_t* count = reinterpret_cast<int32_t*>(w + L.count);
   uint32_t* sup_count = reinterpret_cast<uint32_t*>(w + L.sup_count);
+  uint32_t* n_list = reinterpret_cast<uint32_t*>(w + L.n_list);
   uint2* sup = reinterpret_cast<uint2*>(w + L.sup);
-  Best* part = reinterpret_cast<Best*>(w + L.part);
+  uint2* list = reinterpret_cast<uint2*>(w + L.list);
+  double* val = reinterpret_cast<double*>(w + L.val);
+  const uint32_t cap = (uint32_t)std::min<int64_t>(M * V, 0xFFFFFFFFll);
+  static int sms_of[64] = {0};
+  int dev = 0;
+  W12_CUDA_TRY(cudaGetDevice(&dev));
+  int sms = dev < 64 ? sms_of[dev] : 0;
+  if (sms == 0) {
+    W12_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (dev < 64) sms_of[dev] = sms;
+  }
   // row norms; zero thresholds and counters
-  k_cert_prep<<<(unsigned)M, 256, 0, s>>>(x, K, nx, thr, count, sup_count);
+  k_cert_prep<<<(unsigned)M, 256, 0, s>>>(x, K, nx, thr, count, sup_count, n_list);
   W12_LAUNCH_CHECK("w12_cert_head_argmax: row norms");
   // approximate logits s_v * x.q_v -> thresholds and the candidate superset
   if ((st = i8_gemm_impl(x, M, H->code, H->scale, V, K, nx, H->cbound, thr, sup_count, sup, V, w + L.gemm, L.nx, s,
                          fn)))
     return st;
-  // the two kernels after the GEMM start early (programmatic dependent launch) and wait for
-  // their predecessor's grid before reading its results
+  // The filter is launched plainly: launched early, its blocks would wait beside the GEMM's
+  // CTAs and slow them.  The two kernels after it start early (programmatic dependent
+  // launch) and wait for their predecessor's grid before reading its results.
+  k_cert_filter<<<dim3(kFilterBlocks, (unsigned)M), 256, 0, s>>>(thr, sup_count, sup, (int64_t)V, count, list, n_list);
+  W12_LAUNCH_CHECK("w12_cert_head_argmax: candidates");
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kExactBlocks, (unsigned)M);
-  cfg.blockDim = dim3(kExactWarps * 32);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)(kExactPerSM * sms));
+  cfg.blockDim = dim3(kExactWarps * 32);
   W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_cert_exact, x, K, KC, (const uint8_t*)exact->hi, (const uint8_t*)exact->lo,
                                   (const uint8_t*)exact->base, (const uint32_t*)exact->esc_tile_ptr,
-                                  (const uint32_t*)exact->esc, (const uint32_t*)thr, (const uint32_t*)sup_count,
-                                  (const uint2*)sup, (int64_t)V, count, W12_DECODE_MUL, part));
+                                  (const uint32_t*)exact->esc, (const uint2*)list, (const uint32_t*)n_list, cap,
+                                  W12_DECODE_MUL, val));
   W12_LAUNCH_CHECK("w12_cert_head_argmax: exact logits");
   cfg.gridDim = dim3((unsigned)M);
   cfg.blockDim = dim3(256);
-  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_cert_final, (const Best*)part, (const int32_t*)count, tok, ncand));
+  W12_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_cert_final, (const uint2*)list, (const double*)val, (const uint32_t*)n_list,
+                                  cap, (const int32_t*)count, tok, ncand));
   W12_LAUNCH_CHECK("w12_cert_head_argmax: final");
   return W12_OK;
 }

@@ -18,6 +18,30 @@ int lmhead_argmax_impl(const uint16_t* x, int64_t M, const w12_matrix* head, int
 
 namespace {
 
+// ---- programmatic dependent launch: a kernel launched with launch_pdl may start while the
+// previous kernel on the stream drains (when that kernel signals early); it calls pdl_wait()
+// before it reads anything the previous kernel wrote.  pdl_signal() lets the next kernel
+// start early.  Used only behind small kernels: a waiting block that shares an SM with a
+// long kernel slows it (an LM head's final argmax launched this way cost the head 13 %).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_signal() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+
 // One thread per request.  path_nodes[off .. off+m) doubles as the depth
 // scratch (-1 = not accepted) before it receives the path.
 __device__ void accept_one(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
@@ -59,6 +83,8 @@ __device__ void accept_one(const int32_t* __restrict__ tok, const int32_t* __res
 __global__ void k_accept(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
                          const int32_t* __restrict__ draft, const int32_t* __restrict__ offsets, int32_t n_req, int64_t M,
                          int32_t* path_len, int32_t* path_nodes, int32_t* bonus) {
+  if (threadIdx.x == 0) pdl_signal();
+  pdl_wait();  // the tokens may be the previous kernel's
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n_req; r += gridDim.x * blockDim.x) {
     const int64_t off = offsets ? offsets[r] : 0;
     const int64_t end = offsets ? offsets[r + 1] : M;
@@ -105,8 +131,8 @@ int launch_accept(const int32_t* tok, const int32_t* parent, const int32_t* draf
                   int32_t n_req, int64_t M, int32_t* path_len, int32_t* path_nodes, int32_t* bonus, cudaStream_t s) {
   const int threads = 128;
   const int blocks = (n_req + threads - 1) / threads;
-  k_accept<<<blocks < 1024 ? blocks : 1024, threads, 0, s>>>(tok, parent, draft, offsets, n_req, M, path_len,
-                                                            path_nodes, bonus);
+  W12_CUDA_TRY(launch_pdl(k_accept, dim3(blocks < 1024 ? blocks : 1024), dim3(threads), 0, s, tok, parent, draft,
+                          offsets, n_req, M, path_len, path_nodes, bonus));
   W12_LAUNCH_CHECK("tree acceptance kernel");
   return W12_OK;
 }
@@ -127,6 +153,8 @@ __global__ void __launch_bounds__(256) k_tlv_splice(const int32_t* __restrict__ 
                                                     const uint16_t* __restrict__ x_sub, int64_t n, int64_t K,
                                                     int32_t* parent_out, int32_t* draft_out, int32_t* src_out,
                                                     uint16_t* __restrict__ x_out) {
+  if (threadIdx.x == 0) pdl_signal();
+  pdl_wait();  // the acceptance results may be the previous kernel's
   __shared__ int32_t s_src;
   const int64_t i = blockIdx.x;
   const int32_t L = *path_len;
@@ -188,6 +216,7 @@ __global__ void __launch_bounds__(kBudgetThreads) k_budget_select(const int32_t*
                                                                   int32_t C, int32_t budget, int32_t per_request,
                                                                   int32_t* parent_out, int32_t* draft_out,
                                                                   int32_t* src_out, int32_t* off_out, int32_t* n_kept) {
+  if (threadIdx.x == 0) pdl_signal();  // the row gather that follows starts early
   extern __shared__ uint8_t sm[];
   float* score = reinterpret_cast<float*>(sm);
   int32_t* depth = reinterpret_cast<int32_t*>(score + C);
@@ -279,6 +308,8 @@ __global__ void __launch_bounds__(kBudgetThreads) k_budget_select(const int32_t*
 __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ x, int64_t n_src,
                                                      const int32_t* __restrict__ src, int64_t K,
                                                      uint16_t* __restrict__ out) {
+  if (threadIdx.x == 0) pdl_signal();
+  pdl_wait();  // the source rows may be the previous kernel's
   const int64_t i = blockIdx.x;
   const int32_t s = src[i];
   const uint16_t* row = (s >= 0 && s < n_src) ? x + (int64_t)s * K : nullptr;
@@ -344,9 +375,9 @@ int tlv_splice(const int32_t* path_len, const int32_t* path_nodes, const int32_t
   if (n < 2 || n > (1 << 20) || n_q < 1 || n_q > 0x7FFFFFFF || K < 1 || K > kMaxK)
     return fail(W12_ERR_SHAPE, "tlv_splice: n=%lld (2..2^20), n_q=%lld, K=%lld out of range", (long long)n,
                 (long long)n_q, (long long)K);
-  k_tlv_splice<<<(unsigned)n, 256, 0, (cudaStream_t)stream>>>(path_len, path_nodes, bonus, draft_q, x_q, n_q, sub_parent,
-                                                              sub_draft, x_sub, n, K, parent_out, draft_out, src_out,
-                                                              x_out);
+  W12_CUDA_TRY(launch_pdl(k_tlv_splice, dim3((unsigned)n), dim3(256), 0, (cudaStream_t)stream, path_len, path_nodes,
+                          bonus, draft_q, x_q, n_q, sub_parent, sub_draft, x_sub, n, K, parent_out, draft_out, src_out,
+                          x_out));
   W12_LAUNCH_CHECK("tlv_splice kernel");
   return W12_OK;
 }
@@ -381,7 +412,7 @@ int gather_rows(const uint16_t* x, int64_t n_src, const int32_t* src, int64_t n,
   if (n < 1 || n > 0x7FFFFFFF || n_src < 1 || K < 1 || K > kMaxK)
     return fail(W12_ERR_SHAPE, "gather_rows: n=%lld, n_src=%lld, K=%lld out of range", (long long)n, (long long)n_src,
                 (long long)K);
-  k_gather_rows<<<(unsigned)n, 256, 0, (cudaStream_t)stream>>>(x, n_src, src, K, out);
+  W12_CUDA_TRY(launch_pdl(k_gather_rows, dim3((unsigned)n), dim3(256), 0, (cudaStream_t)stream, x, n_src, src, K, out));
   W12_LAUNCH_CHECK("gather_rows kernel");
   return W12_OK;
 }
