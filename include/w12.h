@@ -95,7 +95,8 @@ typedef enum w12_status {
   W12_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
   W12_ERR_BOUNDS = 5,           /* device data inconsistent with the descriptor (w12_validate,
                                    w12_workspace_status) */
-  W12_ERR_TIMEOUT = 6           /* a GEMM kernel's device-side wait ran out (w12_workspace_status) */
+  W12_ERR_TIMEOUT = 6,          /* a GEMM kernel's device-side wait ran out (w12_workspace_status) */
+  W12_ERR_IO = 7                /* a file could not be read or written, or is not a W12 matrix file */
 } w12_status;
 
 /* A W12 matrix in device memory (layout above).  The struct itself lives in
@@ -124,6 +125,31 @@ W12_API int w12_abi_version(void);
 W12_API int64_t w12_hi_bytes(int64_t N, int64_t K);
 W12_API int64_t w12_lo_bytes(int64_t N, int64_t K);
 W12_API int64_t w12_tile_count(int64_t N, int64_t K);
+
+/* ---- storage (pages: "What's different": the converted layers are stored) */
+
+/* Writes the device matrix A to the file `path`: a 72-byte little-endian header
+ * (magic "W12M", format 1, N, K, n_esc and the byte counts of the five arrays)
+ * followed by the hi plane, the lo plane, base[N], esc_tile_ptr[tile_count+1]
+ * and esc[n_esc], as laid out on the device.  Copies through a bounded host
+ * buffer and synchronises `stream`.  Errors: W12_ERR_INVALID_ARG (null
+ * pointers), W12_ERR_SHAPE, W12_ERR_IO (the file cannot be written),
+ * W12_ERR_CUDA. */
+W12_API int w12_save(const w12_matrix* A, const char* path, void* stream);
+
+/* N, K and n_esc (host pointers) of a file w12_save wrote, so that the caller can
+ * allocate the planes (w12_hi_bytes, w12_lo_bytes, N bytes of bases,
+ * w12_tile_count+1 offsets, n_esc escapes rounded up to a multiple of 4).
+ * Errors: W12_ERR_INVALID_ARG, W12_ERR_IO (no such file, not a W12 matrix file,
+ * a truncated header or sizes that do not match the shape). */
+W12_API int w12_load_info(const char* path, int64_t* N, int64_t* K, int64_t* n_esc);
+
+/* Copies the arrays of the file into the device buffers A describes (A->N,
+ * A->K and A->n_esc must equal the file's); synchronises `stream`.  Errors:
+ * W12_ERR_INVALID_ARG, W12_ERR_SHAPE (the descriptor's sizes differ from the
+ * file's), W12_ERR_IO (unreadable, not a W12 matrix file or truncated),
+ * W12_ERR_CUDA. */
+W12_API int w12_load(const char* path, const w12_matrix* A, void* stream);
 
 /* ---- encode (pages: "What's different", W12 conversion) ----------------- */
 

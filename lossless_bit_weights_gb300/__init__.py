@@ -60,6 +60,10 @@ SIGNATURES = [
     ("w12_decode", ctypes.c_int, [_MP, _P, _P]),
     ("w12_decode_q8", ctypes.c_int, [_MP, _P, _P]),
     ("w12_export_canonical", ctypes.c_int, [_MP, _P, _P, _P, _P, _P]),
+    ("w12_save", ctypes.c_int, [_MP, ctypes.c_char_p, _P]),
+    ("w12_load_info", ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                     ctypes.POINTER(_I64)]),
+    ("w12_load", ctypes.c_int, [ctypes.c_char_p, _MP, _P]),
     ("w12_gemm_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w12_gemm_counter_bytes", _SZ, [_I64]),
     ("w12_gemm", ctypes.c_int, [_P, _I64, _MP, _P, _P, _SZ, _P]),
@@ -197,6 +201,28 @@ def encode(W: torch.Tensor, stream=None) -> W12Matrix:
     esc = torch.empty(esc_alloc_entries(int(n_esc.value)), dtype=torch.int32, device=dev)
     A = W12Matrix(N, K, hi, lo, base, tp, esc, n_esc.value)
     _check(L.w12_encode(_ptr(W), A.desc(), s))
+    return A
+
+
+def w12_save(A: W12Matrix, path: str, stream=None) -> None:
+    """Writes the encoded matrix to a file (w12_save)."""
+    _check(lib().w12_save(A.desc(), os.fsencode(path), _stream(stream)))
+
+
+def w12_load(path: str, device=None, stream=None) -> W12Matrix:
+    """A matrix that w12_save wrote, in new device buffers (w12_load_info, then w12_load)."""
+    L = lib()
+    N, K, n_esc = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(L.w12_load_info(os.fsencode(path), ctypes.byref(N), ctypes.byref(K), ctypes.byref(n_esc)))
+    N, K, n_esc = N.value, K.value, n_esc.value
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    hi = torch.empty(int(L.w12_hi_bytes(N, K)), dtype=torch.uint8, device=dev)
+    lo = torch.empty(int(L.w12_lo_bytes(N, K)), dtype=torch.uint8, device=dev)
+    base = torch.empty(N, dtype=torch.uint8, device=dev)
+    tp = torch.empty(int(L.w12_tile_count(N, K)) + 1, dtype=torch.int32, device=dev)
+    esc = torch.empty(esc_alloc_entries(n_esc), dtype=torch.int32, device=dev)
+    A = W12Matrix(N, K, hi, lo, base, tp, esc, n_esc)
+    _check(L.w12_load(os.fsencode(path), A.desc(), _stream(stream)))
     return A
 
 

@@ -59,6 +59,7 @@ const char* w12_status_string(int s) {
     case W12_ERR_CUDA: return "W12_ERR_CUDA";
     case W12_ERR_BOUNDS: return "W12_ERR_BOUNDS";
     case W12_ERR_TIMEOUT: return "W12_ERR_TIMEOUT";
+    case W12_ERR_IO: return "W12_ERR_IO";
     default: return "W12_ERR_UNKNOWN";
   }
 }

@@ -29,8 +29,8 @@ int i8_gemm_impl(const uint16_t* x, int64_t M, const uint8_t* codes, const float
 namespace {
 
 constexpr int kFilterBlocks = 16;  // blocks per row of the candidate filter
-constexpr int kExactPerSM = 6;     // blocks per SM of the exact recompute
-constexpr int kExactWarps = 10;    // 10 x 8 chunks: K = 5120 in one round
+constexpr int kExactPerSM = 12;    // blocks per SM of the exact recompute
+constexpr int kExactWarps = 5;     // 5 x 8 chunks a round: K = 5120 in two
 
 inline size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256) k_cert_filter(const uint32_t* __restrict_
 // Exact logits of the listed candidates from the W12 head, val[i] for list entry i.  The
 // blocks take the entries i = b, b + gridDim.x, ... (a grid of a few blocks per SM keeps
 // every SM busy whatever the rows' candidate counts); the whole block computes one
-// candidate: lane 4*c8 + t of warp w decodes the 16 columns 16t.. of chunks w*8 + c8 + 80i
+// candidate: lane 4*c8 + t of warp w decodes the 16 columns 16t.. of chunks w*8 + c8 + 40i
 // (the same decode as the GEMM) and patches the channel's escapes in them.  A product of
 // two bf16 values is exact in float; the sum is a float pair (TwoSum), whose error is near
 // 2^-48 of sum|x*w|, far inside the argmax's tie tolerance and on the full-rate float pipe

@@ -109,3 +109,39 @@ def test_error_queries_and_noalloc_check_arguments_before_any_cuda_call():
     assert b"aligned" in lib.w12_last_error()
     assert lib.w12_gemm_noalloc(p, 0, ctypes.byref(A), p, None) == 2
     assert lib.w12_gemm_counter_bytes(5120) == 256 + 768       # error word, then 40 x 4 counters
+
+
+def test_storage_header_checks_without_a_gpu(tmp_path):
+    """w12_load_info / w12_load read and check a file's header on the host: a missing
+    file, a file of another kind, a truncated header or sizes that do not fit the shape
+    are W12_ERR_IO; a descriptor that differs from the file is W12_ERR_SHAPE, before
+    any CUDA call."""
+    import ctypes
+    import struct
+    import lossless_bit_weights_gb300 as w12
+    lib = w12.lib()
+    N_, K_, E_ = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    info = lambda p: lib.w12_load_info(str(p).encode(), ctypes.byref(N_), ctypes.byref(K_), ctypes.byref(E_))
+    assert lib.w12_status_string(7) == b"W12_ERR_IO"
+    assert info(tmp_path / "missing.w12") == 7
+    other = tmp_path / "other.bin"
+    other.write_bytes(b"not a matrix file" * 8)
+    assert info(other) == 7
+    assert b"not a W12" in lib.w12_last_error()
+    N, K, n_esc = 100, 300, 7
+    sizes = [lib.w12_hi_bytes(N, K), lib.w12_lo_bytes(N, K), N, (lib.w12_tile_count(N, K) + 1) * 4, n_esc * 4]
+    header = b"W12M" + struct.pack("<I3q5q", 1, N, K, n_esc, *sizes)
+    assert len(header) == 72
+    good = tmp_path / "good.w12"
+    good.write_bytes(header)
+    assert info(good) == 0 and (N_.value, K_.value, E_.value) == (N, K, n_esc)
+    (tmp_path / "short.w12").write_bytes(header[:40])
+    assert info(tmp_path / "short.w12") == 7
+    bad = tmp_path / "bad.w12"
+    bad.write_bytes(b"W12M" + struct.pack("<I3q5q", 1, N, K, n_esc, sizes[0] + 1, *sizes[1:]))
+    assert info(bad) == 7
+    p = ctypes.c_void_p(256)
+    A = w12.w12_matrix(N, K + 1, 256, 256, 256, 256, 256, n_esc)   # K differs from the file's
+    assert lib.w12_load(str(good).encode(), ctypes.byref(A), None) == 2
+    assert lib.w12_load(None, ctypes.byref(A), None) == 1
+    assert lib.w12_save(None, str(good).encode(), None) == 1

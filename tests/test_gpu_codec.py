@@ -97,3 +97,25 @@ def test_full_size_block_roundtrip(w12):
             assert np.array_equal(esc[rp[r]:rp[r + 1]], enc.esc[enc.rowptr[i]:enc.rowptr[i + 1]])
         del Wd, A, dec, c
         torch.cuda.empty_cache()
+
+
+def test_save_and_load_round_trip(w12, tmp_path):
+    """An encoded matrix written by w12_save and read back by w12_load has the same
+    planes, bases, escape index and escapes, and gives the same GEMM bit for bit; a
+    truncated file is refused."""
+    import ctypes
+    W = synth.weights(4, 0, 3, 700, 1000)
+    A = w12.encode(to_dev16(W))
+    path = tmp_path / "m.w12"
+    w12.w12_save(A, str(path))
+    B = w12.w12_load(str(path))
+    assert (B.N, B.K, B.n_esc) == (A.N, A.K, A.n_esc)
+    for name in ("hi", "lo", "base", "esc_tile_ptr"):
+        assert torch.equal(getattr(A, name), getattr(B, name)), name
+    assert torch.equal(A.esc[:A.n_esc], B.esc[:B.n_esc])
+    x = to_dev16(synth.activations(5, 0, 7, 16, 1000))
+    assert torch.equal(w12.w12_gemm(x, A), w12.w12_gemm(x, B))
+    data = path.read_bytes()
+    cut = tmp_path / "cut.w12"
+    cut.write_bytes(data[:-5])
+    assert w12.lib().w12_load(str(cut).encode(), B.desc(), None) == 7
