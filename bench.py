@@ -48,8 +48,8 @@ METRIC = "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (34816x5120, M=16)
 # from an ncu capture, with the SHA-256 of the GEMM kernel's sources it was taken on: the
 # line reports the traffic only while those sources are unchanged.
-TRAFFIC_GATE_UP_M16 = 273629184 + 4154368
-TRAFFIC_SOURCES_SHA256 = "3e114b0db094012400de05fc5b6f95e44caf647e3c09a36aabfc06abc118bd24"
+TRAFFIC_GATE_UP_M16 = 273648896 + 4253696
+TRAFFIC_SOURCES_SHA256 = "7c7df2725ac43f8643591ca46837ce7f5b4250493bfafa18546a099726e8370d"
 GEMM_SOURCES = ("lossless_bit_weights_gb300/csrc/w12_gemm.cu", "lossless_bit_weights_gb300/csrc/w12_internal.cuh")
 
 
@@ -948,6 +948,44 @@ def extra_rows(w12, synth, torch, mats, xs, ws, M, args, hbm):
                                "step_us": 1e3 * (min(ms_v, ms_wy) + ms_c),
                                "snapshot_bytes_avoided": n_l * nn * Hg * dg * dg * 4,
                                "status": int(st_g.item())}
+
+    # ---- context: torch bf16 matmul (cuBLAS) over the block's four shapes, the same weights
+    # as plain bf16 (2 B per weight, nothing to decode), bf16 outputs, launched back to back
+    # like the W12 block on the same inputs; the block's 660 MB of bf16 exceed the L2
+    Wb = []
+    for tensor, (_, A) in enumerate(mats):
+        W = torch.empty((A.N, A.K), dtype=torch.int16, device=dev)
+        synth.weights_dev(0, 0, tensor, W)
+        Wb.append(W.view(torch.bfloat16))
+    wsc = w12.Workspace(dev)
+    wsc.get(max(w12.gemm_workspace_size(192, A.N, A.K) for _, A in mats))
+    ctx = {"weights": "the block's bf16 weights (layer 0)", "outputs": "bf16 (cuBLAS), fp32 (W12)"}
+    for Mc in (16, 32, 192):
+        xc = []
+        for tensor, (_, A) in enumerate(mats):
+            x = torch.empty((Mc, A.K), dtype=torch.int16, device=dev)
+            synth.activations_dev(1, 0, tensor, x)
+            xc.append(x)
+        yb16 = [torch.empty((Mc, A.N), dtype=torch.bfloat16, device=dev) for _, A in mats]
+        y32 = [torch.empty((Mc, A.N), dtype=torch.float32, device=dev) for _, A in mats]
+
+        def cublas_block():
+            for W, x, y in zip(Wb, xc, yb16):
+                torch.mm(x.view(torch.bfloat16), W.t(), out=y)
+
+        def w12_block():
+            for (_, A), x, y in zip(mats, xc, y32):
+                w12.w12_gemm(x, A, y=y, ws=wsc)
+
+        ms_cb = timed_ms(torch, cublas_block, steps)
+        ms_w = timed_ms(torch, w12_block, steps)
+        cb_bytes = sum(2 * A.N * A.K + 2 * Mc * A.K + 2 * Mc * A.N for _, A in mats)
+        ctx[f"m{Mc}"] = {"cublas_bf16_us": 1e3 * ms_cb, "w12_us": 1e3 * ms_w, "w12_speedup": ms_cb / ms_w,
+                         "cublas_stream_GBps": cb_bytes / (ms_cb * 1e-3) / 1e9,
+                         "cublas_frac_hbm": cb_bytes / (ms_cb * 1e-3) / 1e9 / hbm}
+    out["cublas_bf16_block_context"] = ctx
+    del Wb
+    torch.cuda.empty_cache()
     return out
 
 

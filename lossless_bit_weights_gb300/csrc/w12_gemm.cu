@@ -155,18 +155,22 @@ constexpr int kABuf = kBlockTiles * kTileRows * 128;  // decoded 128x64 bf16 blo
 //            scheduler and it finished its equal share ~6 us sooner on gate/up (a launch
 //            ends with the slower one); as two pipelines of one CTA they finish together.
 //  kModeOne  (NT >= 64 on short matrices, and 256): one pipeline per CTA; its x chunks are
-//            large.
+//            large.  At NT = 192 the rows split between CTAs are summed after the launch
+//            (k_slot_sum).
 //  kModePair (up to 192 tokens on matrices with a row block per SM or more): two pipelines
 //            share one range of row-block pairs x 64 columns, pipeline p on row block
 //            2*pair + p, and one x warp and ring (each stage freed by both MMA issuers).
 //            Against kModeOne: twice the decode warps per SM; against kModeOwn: one x
 //            stream for both pipelines and deeper record rings.  Stream-K splits run over
 //            twice as many CTAs per (longer) row, so it pays on tall matrices only.
-enum { kModeOwn = 0, kModeOne = 1, kModePair = 2 };
+//  kModePairSum (64 to 192 tokens on shorter matrices with long rows): kModePair's CTA, but
+//            the rows split between CTAs are summed after the launch over every SM
+//            (k_slot_sum), not by each row's last part.
+enum { kModeOwn = 0, kModeOne = 1, kModePair = 2, kModePairSum = 3 };
 
 template <int NT, bool Q8, int MODE>
 struct TcPlan {
-  static constexpr bool kWide = MODE == kModePair;
+  static constexpr bool kWide = MODE == kModePair || MODE == kModePairSum;
   static constexpr int kPipes = MODE == kModeOne ? 1 : 2;
   static constexpr int kParts = MODE == kModeOwn ? 2 : 1;     // places in the partition per CTA
   static constexpr int kGroups = 2;
@@ -187,7 +191,7 @@ struct TcPlan {
   static constexpr int kX = NT * 128;                         // swizzled x chunk, 1 KB multiple
   // x stages: at 192 tokens with row-block pairs a third 24 KB stage (shared by both
   // pipelines) measured better than a fourth record stage per pipeline
-  static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : (MODE == kModePair && NT == 192) ? 3 : 2;
+  static constexpr int kXStages = NT <= 16 ? 4 : NT <= 64 ? 3 : (kWide && NT == 192) ? 3 : 2;
   // A buffers (decoded 128x64 tiles) in rotation over the pipeline's units: with more than
   // one per decode group, a group stores a unit while the MMA of the unit before its previous
   // one may still run.  At 16 tokens with own ranges a fifth record stage measured better
@@ -365,6 +369,11 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
   static_assert(!I8 || Q8, "INT8 codes use the 8-bit record plan");
   constexpr int S = P::kStages, SX = P::kXStages, kTcGroups = P::kGroups, AB = P::kABufs;
   constexpr int kTcProducer = P::kProducer, kTcMma = P::kMma, kTcPub = P::kPub, kTcX = P::kXWarp;
+  // storing y with pairs summed after, or one pipeline per CTA at 192 tokens (96 KB slots):
+  // a row block split between CTAs is summed after the launch (k_slot_sum, over every SM)
+  // instead of by its last part alone.  With one pipeline at 64 and 128 tokens the extra
+  // launch cost more than the fix-up it saves.
+  constexpr bool kDefer = EPI == EPI_STORE && ((MODE == kModeOne && NT == 192) || MODE == kModePairSum);
   extern __shared__ __align__(1024) uint8_t smem_cta[];
   const int lane = threadIdx.x & 31, gwarp = threadIdx.x >> 5;
   // pipeline and the warp's role index inside it: the decode warps of pipeline p are
@@ -640,7 +649,7 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
     // tiles and, when it is their last arrival, adds the parts' slots.
     const int KC = (int)a.KC, U0 = (int)u0;
     const int srb0 = U0 / KC;
-    if (nunp > 0 && (U0 % KC) != 0 && (U0 + nunp - 1) / KC > srb0) {
+    if (!kDefer && nunp > 0 && (U0 % KC) != 0 && (U0 + nunp - 1) / KC > srb0) {
       if (!warp_wait(pub, 0u)) {
         bail = true;
       } else {
@@ -830,7 +839,9 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
           tc_fence_before();
           mbar_arrive(abuf ? epi0 + 8 : acc_empty);
           if (lane == 0) atomicAdd(misc + 15, 1u);
-          if (P::kHasPub && j != nunp - 1) {
+          if (kDefer) {
+            // the parts' slots are added after the launch
+          } else if (P::kHasPub && j != nunp - 1) {
             // A partial row that ends before the range does is the range's first: the
             // publisher warp publishes it, and this group goes on decoding.  The barrier's
             // release orders each thread's slot stores before the publisher's increment.
@@ -1018,21 +1029,25 @@ int device_sms(int* sms) {
 struct LaunchShape {
   int nt, mode, parts;
 };
-LaunchShape launch_shape(int64_t M, int64_t N, int sms) {
+LaunchShape launch_shape(int64_t M, int64_t N, int64_t K, int sms) {
   const int nt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : M <= 192 ? 192 : 256;
+  const int64_t RB = row_blocks(N);
   // up to 32 tokens: row-block pairs on tall matrices (a row block per SM or more), else two
   // pipelines with their own ranges
-  if (nt <= 32) return row_blocks(N) >= sms ? LaunchShape{nt, kModePair, 1} : LaunchShape{nt, kModeOwn, 2};
+  if (nt <= 32) return RB >= sms ? LaunchShape{nt, kModePair, 1} : LaunchShape{nt, kModeOwn, 2};
   // row-block pairs: on matrices with a row block per SM or more, up to 192 tokens (at 256
   // a pipeline's record ring would drop to three stages)
-  const bool pair = nt <= 192 && row_blocks(N) >= sms;
-  return {nt, pair ? kModePair : kModeOne, 1};
+  if (nt <= 192 && RB >= sms) return {nt, kModePair, 1};
+  // shorter matrices: pairs summed after the launch where a CTA still gets 24 pair units or
+  // more (long rows), else one pipeline per CTA
+  if (nt <= 192 && ((RB + 1) / 2) * k_chunks(K) >= 24 * (int64_t)sms) return {nt, kModePairSum, 1};
+  return {nt, kModeOne, 1};
 }
 
 // Units of the partition: row block x 64 columns, or row-block pair x 64 columns.
 int64_t partition_units(int64_t N, int64_t K, int mode) {
   const int64_t RB = row_blocks(N), KC = k_chunks(K);
-  return (mode == kModePair ? (RB + 1) / 2 : RB) * KC;
+  return (mode == kModePair || mode == kModePairSum ? (RB + 1) / 2 : RB) * KC;
 }
 
 // CTAs of the stream-K partition for a T-unit problem.
@@ -1052,10 +1067,10 @@ struct WsLayout {
 
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool argmax, int sms) {
   const int64_t RB = row_blocks(N), RT = row_tiles(N), KC = k_chunks(K), T = RB * KC;
-  const LaunchShape ls = launch_shape(M, N, sms);
+  const LaunchShape ls = launch_shape(M, N, K, sms);
   const int64_t TP = partition_units(N, K, ls.mode);
   const int64_t G = partition_ctas(TP, sms, ls.parts);
-  const int64_t n_slots = ls.mode == kModePair ? 2 * ((RB + 1) / 2 + G) : RB + G;
+  const int64_t n_slots = ls.mode == kModePair || ls.mode == kModePairSum ? 2 * ((RB + 1) / 2 + G) : RB + G;
   WsLayout L{};
   L.error = 0;
   L.counters = 256;
@@ -1126,7 +1141,15 @@ int launch_tc(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
 
 template <bool Q8, int EPI>
 int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
-  const bool pair = ls.mode == kModePair;
+  // pairs summed after the launch store y; for the other outputs they are plain pairs
+  const bool pair = ls.mode == kModePair || (ls.mode == kModePairSum && EPI != EPI_STORE);
+  if constexpr (EPI == EPI_STORE) {
+    if (ls.mode == kModePairSum) {
+      if (ls.nt == 64) return launch_tc<64, Q8, kModePairSum, EPI>(map, a, s);
+      if (ls.nt == 128) return launch_tc<128, Q8, kModePairSum, EPI>(map, a, s);
+      return launch_tc<192, Q8, kModePairSum, EPI>(map, a, s);
+    }
+  }
   switch (ls.nt) {
     case 16: return pair ? launch_tc<16, Q8, kModePair, EPI>(map, a, s) : launch_tc<16, Q8, kModeOwn, EPI>(map, a, s);
     case 32: return pair ? launch_tc<32, Q8, kModePair, EPI>(map, a, s) : launch_tc<32, Q8, kModeOwn, EPI>(map, a, s);
@@ -1137,6 +1160,46 @@ int launch_nt(const LaunchShape& ls, const CUtensorMap& map, const GemmArgs& a, 
       return pair ? launch_tc<192, Q8, kModePair, EPI>(map, a, s) : launch_tc<192, Q8, kModeOne, EPI>(map, a, s);
     default: return launch_tc<256, Q8, kModeOne, EPI>(map, a, s);
   }
+}
+
+// y of the rows that a launch split between CTAs: the parts' slots added in part order from
+// zero, as the in-kernel fix-up adds them.  Block (row tile, group of 8 token quads); thread
+// (lane = channel of the row tile, quad).  Row blocks held by one part were stored by the GEMM.
+__global__ void __launch_bounds__(256) k_slot_sum(const float* __restrict__ slots, float* __restrict__ y,
+                                                  int64_t ldy, int64_t N, int M, int nt, int64_t KC, int64_t G,
+                                                  int64_t T, bool wide) {
+  // the next GEMM may start streaming its weights; it reads x only after this grid completes
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ int64_t parts[2];
+  const int64_t rt = blockIdx.x, rb = rt / kBlockTiles;
+  const int tl = (int)(rt % kBlockTiles);
+  // row of the partition: the row block, or with row-block pairs the pair (pipeline rb & 1)
+  const int64_t srb = wide ? rb >> 1 : rb;
+  if (threadIdx.x == 0) {
+    parts[0] = cta_of_unit(srb * KC, G, T);
+    parts[1] = cta_of_unit((srb + 1) * KC - 1, G, T);
+  }
+  __syncthreads();
+  const int64_t cf = parts[0], cl = parts[1];
+  const int lane = threadIdx.x & 31, q = (int)blockIdx.y * 8 + (threadIdx.x >> 5), tok = 4 * q;
+  const int64_t n = rt * kTileRows + lane;
+  if (cf == cl || tok >= M || n >= N) return;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t c = cf; c <= cl; ++c) {
+    // slot of (part c, row block rb): [row tile][token quad][lane] float4
+    const int64_t slot = wide ? 2 * (c + srb) + (rb & 1) : c + srb;
+    const float4 p =
+        __ldcg(reinterpret_cast<const float4*>(slots + (slot * kBlockTiles + tl) * (int64_t)nt * 32) + q * 32 + lane);
+    v.x += p.x;
+    v.y += p.y;
+    v.z += p.z;
+    v.w += p.w;
+  }
+  float* yo = y + (int64_t)tok * ldy + n;
+  yo[0] = v.x;
+  if (tok + 1 < M) yo[ldy] = v.y;
+  if (tok + 2 < M) yo[2 * ldy] = v.z;
+  if (tok + 3 < M) yo[3 * ldy] = v.w;
 }
 
 // Host-side checks of a GEMM call's arguments (everything but the workspace); a call that
@@ -1193,7 +1256,7 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
   a.N = A->N;
   a.KC = KC;
   a.RB = RB;
-  const LaunchShape ls = launch_shape(M, A->N, sms);
+  const LaunchShape ls = launch_shape(M, A->N, A->K, sms);
   a.T = partition_units(A->N, A->K, ls.mode);
   a.G = partition_ctas(a.T, sms, ls.parts);
   a.ldy = A->N;
@@ -1217,6 +1280,13 @@ int run_gemm(const uint16_t* x, int64_t M, const w12_matrix* A, float* y, int32_
     } else if (!argmax) {
       a.y = y + m0 * A->N;
       st = q8 ? launch_nt<true, EPI_STORE>(ls, map, a, s) : launch_nt<false, EPI_STORE>(ls, map, a, s);
+      if (!st && ((ls.mode == kModeOne && ls.nt == 192) || ls.mode == kModePairSum)) {
+        // plain launch: it starts when the GEMM's grid has completed
+        // 8 token quads per block (nt is a multiple of 32 here); fewer than 2^31 row tiles
+        const dim3 grid((unsigned)(RB * kBlockTiles), (unsigned)(ls.nt / 32));
+        k_slot_sum<<<grid, 256, 0, s>>>(a.slots, a.y, a.ldy, A->N, Mg, ls.nt, KC, a.G, a.T, ls.mode == kModePairSum);
+        W12_LAUNCH_CHECK("w12 gemm: split row blocks");
+      }
     } else {
       st = q8 ? launch_nt<true, EPI_ARGMAX>(ls, map, a, s) : launch_nt<false, EPI_ARGMAX>(ls, map, a, s);
     }

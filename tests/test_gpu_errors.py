@@ -5,7 +5,8 @@
   frees its tensor memory; w12_workspace_status then reports W12_ERR_TIMEOUT and clears
   the workspace, and the next call on the same workspace gives the full result, in every
   launch mode (two pipelines with their own ranges at 16 tokens, one pipeline at 192 tokens
-  on a short matrix, row-block pairs at 64 and 192 tokens on tall ones).  No GPU fault is
+  on a short matrix, row-block pairs at 64 and 192 tokens on tall ones, pairs summed after
+  the launch at 100 tokens on long rows).  No GPU fault is
   involved: the kernels return normally.
 - A damaged escape index: w12_validate reports W12_ERR_BOUNDS for index arrays corrupted
   on the host (copies of a valid matrix's); such a matrix is never given to a GEMM.
@@ -33,7 +34,8 @@ def w12():
     return m
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 5120, 5120), (192, 2048, 5120), (64, 20480, 1024), (192, 20480, 1024)])
+@pytest.mark.parametrize("M,N,K", [(16, 5120, 5120), (192, 2048, 5120), (64, 20480, 1024), (192, 20480, 1024),
+                                   (100, 5120, 17408)])
 def test_wait_timeout_is_reported_and_the_workspace_recovers(w12, M, N, K):
     layer = 11
     Wd = device_weights(0, layer, M, N, K)

@@ -72,6 +72,24 @@ def test_many_parts_per_row_block(w12, M, N, K, q8):
     assert ws.status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,q8", [(65, 1100, 46789, False), (65, 1100, 46789, True), (150, 1300, 40000, False)])
+def test_pairs_summed_after_the_launch(w12, M, N, K, q8):
+    """64 to 192 tokens on a matrix with fewer row blocks than SMs and long rows: row-block
+    pairs whose split rows are summed by a second kernel over every SM.  Odd row-block
+    counts (the last pair has one row block), a ragged last row block, ragged K (x padded)
+    and ragged tokens; every element against the oracle, and repeats bit-identical."""
+    W = synth.weights(5, M, N * 3 + K, N, K)
+    x = synth.activations(6, M, K, M, K)
+    ws = w12.Workspace()
+    check(w12, W, x, q8, ws=ws)
+    A = w12.encode(to_dev16(W))
+    fn = w12.w12_gemm_q8 if q8 else w12.w12_gemm
+    y0 = fn(to_dev16(x), A, ws=ws)
+    y1 = fn(to_dev16(x), A, ws=ws)
+    assert torch.equal(y0, y1)
+    assert ws.status() == 0
+
+
 def test_exact_on_small_integers(w12):
     """Integer-valued weights and activations with small magnitudes: every
     partial sum is exact in fp32, so the GPU result equals the integer GEMM."""
@@ -101,8 +119,8 @@ def test_deterministic_repeats(w12):
 
 @pytest.mark.parametrize("M", [32, 100, 192, 256])
 def test_deterministic_repeats_wide(w12, M):
-    """Back-to-back launches on a full-size gate/up matrix at 32 tokens (two pipelines per
-    CTA), 100 (row-block pairs), 192 and 256 (one pipeline, shallow record rings): every
+    """Back-to-back launches on a full-size gate/up matrix at 32, 100 and 192 tokens
+    (row-block pairs) and 256 (one pipeline, shallow record rings): every
     launch gives the same bits (the stream-K sums run in a fixed order), and a sample of
     channels matches the oracle."""
     N, K = 34816, 5120
