@@ -40,7 +40,10 @@
  *    touched only after it completes.  A kernel that signals early
  *    (griddepcontrol.launch_dependents) must therefore not write the matrix
  *    a following GEMM reads.  Kernels that do not signal, such as the
- *    encoders here, complete before the GEMM starts.
+ *    encoders here, complete before the GEMM starts.  From 64 tokens on, a
+ *    call that stores y may add a second kernel, launched plainly after the
+ *    GEMM's grid, that adds the rows the GEMM split between CTAs; it signals
+ *    early too and writes only y.
  *  - bf16 tensors are passed as uint16_t bit patterns.
  *  - Shapes: 1 <= N, 1 <= K <= 65535 (the escape entry keeps the column in 16
  *    bits and reserves the all-ones column), 1 <= M.
