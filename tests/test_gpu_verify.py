@@ -121,6 +121,21 @@ def test_lmhead_tiny(w12, q8):
     check_paths(pl, pn, bo, tok, parent, draft, np.array([0, 8]))
 
 
+@pytest.mark.parametrize("q8", [False, True])
+def test_lmhead_short_long_rows(w12, q8):
+    """A 1100 x 46789 head at 65 tokens: fewer row blocks than SMs, long rows and an odd
+    row-block count, so the launch takes row-block pairs with the fused argmax (its split
+    rows reduced in the kernel); tokens against the fp64 logits."""
+    V, K, M = 1100, 46789, 65
+    Wh = synth.weights(2, 0, 19, V, K)
+    x = synth.activations(2, 0, 119, M, K)
+    A = w12.encode(to_dev16(Wh))
+    enc = oracle.encode(Wh)
+    y64 = oracle.gemm(x, oracle.decode_q8(enc) if q8 else oracle.decode(enc), with_bound=False)
+    tok = w12.w12_lmhead_argmax(to_dev16(x), A, q8=q8).cpu().numpy()
+    argmax_check(tok, y64)
+
+
 HEAD = (151936, 5120)   # the LM head of the 27B-class configs: vocab x hidden
 
 
