@@ -49,7 +49,7 @@ METRIC = "W12 verify-GEMM decoded-weight GB/s (27B-class block, M=16)"
 # from an ncu capture, with the SHA-256 of the GEMM kernel's sources it was taken on: the
 # line reports the traffic only while those sources are unchanged.
 TRAFFIC_GATE_UP_M16 = 273648896 + 4253696
-TRAFFIC_SOURCES_SHA256 = "7c7df2725ac43f8643591ca46837ce7f5b4250493bfafa18546a099726e8370d"
+TRAFFIC_SOURCES_SHA256 = "cdf8af2e23f63f0522e401ba7f4510d5b381c677d4875ca97d002cd59879b4a1"
 GEMM_SOURCES = ("lossless_bit_weights_gb300/csrc/w12_gemm.cu", "lossless_bit_weights_gb300/csrc/w12_internal.cuh")
 
 

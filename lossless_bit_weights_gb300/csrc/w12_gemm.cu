@@ -722,10 +722,10 @@ __global__ void __launch_bounds__(TcPlan<NT, Q8, MODE>::kBoundThreads, TcPlan<NT
       }
       // The full barrier's parity wait is exact only while this stage's previous unit
       // (j - S) has already been consumed.  That holds when it is this group's own unit (S
-      // even) or at least five back (the other group has finished unit j - 5 by now: this
-      // group's previous A buffer was freed by the MMA of unit j - 4, issued after that of
-      // j - 5).  A three-stage ring waits for the release of unit j - 3 first.
-      if (S % 2 == 1 && S < 5 && j >= S && !warp_wait(rec_empty0 + 8 * s, ph ^ 1u)) {
+      // even) or AB + 2 or more back: this group's previous unit waited for the MMA of unit
+      // j - 2 - AB, which followed the decode of every unit up to it.  A shorter odd ring
+      // (three stages with two A buffers) waits for the release of unit j - S first.
+      if (S % 2 == 1 && S < AB + 2 && j >= S && !warp_wait(rec_empty0 + 8 * s, ph ^ 1u)) {
         bail = true;
         break;
       }
