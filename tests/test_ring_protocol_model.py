@@ -16,6 +16,12 @@ group finished unit j - 2 after the MMA of unit j - 2 - AB, which followed the d
 every unit up to it); otherwise the group first waits for that unit's release.  The plans below are the (S, AB, SX) of every k_gemm_tc
 instantiation (TcPlan: 12-bit and 8-bit records, NT 16..256, all launch modes); the planted
 cases drop the release wait where it is needed and must go stale.
+
+The accumulator hand-off is modelled too: a segment (a row block's units in the range) ends
+with its last MMA's commit to the accumulator barrier; the group that decoded the segment's
+last unit waits until the earlier segments are drained (a counter), then for the
+accumulator, drains it and releases it; the issuer waits for that release before the first
+MMA of the segment that reuses the accumulator (one or two of them).
 """
 import heapq
 import random
@@ -66,6 +72,12 @@ class Sim:
             return
         if op[0] == "delay":
             self.at(self.t + op[1], lambda: self.step(actor))
+        elif op[0] == "count":  # ("count", counter, n): wait until the counter reaches n
+            _, b, n = op
+            if self.done.get(b, 0) >= n:
+                self.at(self.t, lambda: self.step(actor))
+            else:
+                self.waiters.setdefault(b, []).append((n - 1, actor))
         else:  # ("wait", barrier, k): wait for the k-th completion (0-based) by parity
             _, b, k = op
             c = self.done.get(b, 0)
@@ -84,9 +96,19 @@ class Sim:
             fn()
 
 
-def simulate(S, AB, SX, release_wait, n_units, seed):
+def simulate(S, AB, SX, release_wait, n_units, seed, KC=None, kc0=0, acc_bufs=1, drain_count=True):
+    """KC: units per row block (None: one segment); kc0: the first unit's chunk; a segment
+    (the units of one row block) ends with a drain of the accumulator by the group that
+    decoded its last unit, after the drains of the earlier segments (drain_count)."""
     sim = Sim(random.Random(seed))
     mma_end = [0.0]
+    KC = KC or n_units + kc0
+
+    def seg_of(j):
+        return (kc0 + j) // KC - kc0 // KC
+
+    def last_of_seg(j):
+        return (kc0 + j) % KC == KC - 1 or j == n_units - 1
 
     def producer():
         for j in range(n_units):
@@ -116,14 +138,27 @@ def simulate(S, AB, SX, release_wait, n_units, seed):
                 yield ("wait", ("a_empty", j % AB), j // AB - 1)
             yield ("delay", sim.lat(0.5, 3.0))           # decode and store the A tile
             sim.complete(("a_full", j % AB))
+            if last_of_seg(j):                           # drain the segment's accumulator
+                seg = seg_of(j)
+                if drain_count and seg > 0:
+                    yield ("count", "drains", seg)
+                yield ("wait", ("acc_full", seg % acc_bufs), seg // acc_bufs)
+                yield ("delay", sim.lat(0.3, 2.0))
+                sim.complete(("acc_empty", seg % acc_bufs))
+                sim.complete("drains")
 
     def issuer():
         for j in range(n_units):
+            seg = seg_of(j)
+            if (j == 0 or (kc0 + j) % KC == 0) and seg >= acc_bufs:   # the accumulator drained
+                yield ("wait", ("acc_empty", seg % acc_bufs), seg // acc_bufs - 1)
             yield ("wait", ("a_full", j % AB), j // AB)
             yield ("wait", ("x_full", j % SX), j // SX)
             end = max(mma_end[0], sim.t) + sim.lat(0.1, 1.5)   # MMAs finish in issue order
             mma_end[0] = end
             sim.at(end, lambda j=j: (sim.complete(("a_empty", j % AB)), sim.complete(("x_empty", j % SX))))
+            if last_of_seg(j):
+                sim.at(end, lambda seg=seg: sim.complete(("acc_full", seg % acc_bufs)))
             yield ("delay", 0.02)
 
     sim.run([producer(), xloader(), group(0), group(1), issuer()])
@@ -152,3 +187,25 @@ def test_planted_missing_release_wait_goes_stale(S, AB):
 def test_rings_at_the_bound_need_no_release_wait(S, AB):
     """Odd rings of AB + 2 stages or more, and even rings, stay exact without the wait."""
     assert all(simulate(S, AB, 3, False, 160, seed) == 0 for seed in range(40))
+
+
+@pytest.mark.parametrize("S,AB,SX", [(5, 2, 4), (4, 3, 3), (3, 2, 3), (7, 4, 2), (8, 2, 3)])
+@pytest.mark.parametrize("acc_bufs", [1, 2])
+def test_accumulator_handoff_waits_exactly(S, AB, SX, acc_bufs):
+    """Row blocks of 1 to 9 units starting anywhere in the range: the MMA issuer waits for
+    the drain of the accumulator's previous segment, and the group ending a segment waits
+    for the drains before it, then for the accumulator; every such wait is exact."""
+    rng = random.Random(S * 100 + AB * 10 + acc_bufs)
+    for seed in range(30):
+        KC = rng.randint(1, 9)
+        kc0 = rng.randrange(KC)
+        assert simulate(S, AB, SX, kernel_release_wait(S, AB), 120, seed, KC, kc0, acc_bufs) == 0, seed
+
+
+def test_planted_drains_out_of_order_go_stale():
+    """Without the count of earlier drains, a group ending a short segment can wait for the
+    accumulator a phase early (the segment before has not been committed yet)."""
+    stale = 0
+    for seed in range(60):
+        stale += simulate(5, 2, 4, False, 120, seed, KC=2, kc0=1, acc_bufs=1, drain_count=False) > 0
+    assert stale > 0
